@@ -1,0 +1,400 @@
+"""Pins for the CPU oracle against facts fixed by the pages or by mathematics.
+
+None of these tests re-types the oracle's own formulas: each checks a
+hand-worked value, a closed form, an exact-arithmetic result, a brute-force
+count or an invariant, chosen so that a dropped term, a swapped operand or a
+wrong sign or index in the oracle fails at least one of them.
+
+Sources: "Lion Cub: Minimizing Communication Overhead in Distributed Lion"
+(machine review page: "What carries the argument", Eq. (1), the assumptions
+list on the alternating-sign rule and Fig. 10, the quoted body text on tied
+majority votes) and "Communication Efficient Distributed Training with
+Distributed Lion" (summary page, "Approach").
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32(x):
+    return np.float32(x)
+
+
+# ---------------------------------------------------------------------------
+# Eq. (1): L1 quantization
+# ---------------------------------------------------------------------------
+
+def _golden_q1():
+    with open(os.path.join(GOLDEN, "q1_hand_vectors.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden_q1()["cases"], ids=lambda c: c["name"])
+def test_q1_hand_vectors(oracle_lib, case):
+    x = np.array(case["x"], dtype=np.float32)
+    m1 = oracle.m1(x)
+    expect_m1 = np.float32(case["m1_num"] / case["m1_den"])
+    assert m1 == expect_m1
+    q = oracle.q1(x, case["nbits"])
+    assert q.tolist() == case["q"]
+    words = oracle.pack_codes(q, case["nbits"])
+    assert [int(h, 16) for h in case["packed_hex"]] == words.tolist()
+
+
+def test_q1_two_workers_per_worker_m1(oracle_lib):
+    """Each worker scales by its own M1; the integer codes are summed."""
+    g = _golden_q1()["two_workers"]
+    d = len(g["c0"])
+    # beta1 = 0 makes c equal to the gradient exactly (0*m + 1*g).
+    grads = [np.array(g["c0"], np.float32), np.array(g["c1"], np.float32)]
+    theta = np.zeros(d, np.float32)
+    m = [np.zeros(d, np.float32), np.zeros(d, np.float32)]
+    out = oracle.step(d=d, W=2, layout=None, beta1=0.0, beta2=0.5, lr=1.0, wd=0.0,
+                      mode=oracle.MODE_L1, nbits=g["nbits"], flags=0, sync_interval=0, t=0,
+                      grads=grads, theta=theta, m=m)
+    assert out.agg.tolist() == g["agg"]
+    assert [oracle.code_sum(out.wire, g["nbits"], e) for e in range(d)] == g["agg"]
+    # theta = 0 - 1*(sign(agg) + 0)
+    assert theta.tolist() == [-float(np.sign(a)) for a in g["agg"]]
+
+
+def _exact_q1(x, nbits):
+    """Eq. (1) in exact rational arithmetic, Python's round() = ties to even."""
+    qmax = 2 ** (nbits - 1) - 1
+    xs = [Fraction(float(v)) for v in x]
+    m1 = sum(abs(v) for v in xs) / len(xs)
+    if m1 == 0:
+        return [0] * len(xs), [Fraction(0)] * len(xs)
+    ys = [qmax * v / m1 for v in xs]
+    return [max(-qmax, min(qmax, round(y))) for y in ys], ys
+
+
+@pytest.mark.parametrize("nbits", [2, 4, 8])
+def test_q1_matches_exact_rational(oracle_lib, nbits):
+    """fp32 Q1 equals exact-arithmetic Q1 wherever y is not within fp32 rounding
+    error of a rounding boundary (k + 1/2)."""
+    rng = np.random.default_rng(1234 + nbits)
+    checked = 0
+    for trial in range(40):
+        n = int(rng.integers(1, 200))
+        x = (rng.laplace(size=n) * 10.0 ** rng.integers(-4, 3)).astype(np.float32)
+        q = oracle.q1(x, nbits)
+        qe, ys = _exact_q1(x, nbits)
+        for e in range(n):
+            frac = abs(ys[e]) - math.floor(abs(ys[e]))
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 10 ** 5) * (1 + abs(ys[e])):
+                continue
+            assert q[e] == qe[e], (trial, e, float(ys[e]))
+            checked += 1
+    assert checked > 1000
+
+
+def test_q1_range_and_sign(oracle_lib):
+    rng = np.random.default_rng(7)
+    x = (rng.standard_t(2.5, size=5000) * 1e-3).astype(np.float32)
+    for nbits in (2, 4, 8):
+        qmax = 2 ** (nbits - 1) - 1
+        q = oracle.q1(x, nbits).astype(np.int64)
+        assert q.max() <= qmax and q.min() >= -qmax
+        # the code never has the opposite sign of x
+        assert np.all(q * np.sign(x) >= 0)
+
+
+# ---------------------------------------------------------------------------
+# M1: mean absolute value, fp64 accumulation
+# ---------------------------------------------------------------------------
+
+def test_m1_against_exact_sum(oracle_lib):
+    rng = np.random.default_rng(5)
+    for n in (1, 2, 31, 1000, 100_003):
+        x = (rng.standard_t(3.0, size=n) * 1e-3).astype(np.float32)
+        exact = Fraction(math.fsum(abs(float(v)) for v in x)) / n
+        got = oracle.m1(x)
+        # correctly rounded value of the exact mean, within one fp32 ulp
+        ref = np.float32(float(exact))
+        assert abs(float(got) - float(ref)) <= float(np.spacing(ref)), (n, got, ref)
+
+
+def test_m1_exact_when_sum_is_exact(oracle_lib):
+    x = np.array([0.5, -0.25, 0.125, -1.0, 2.0, -0.0, 0.0, 4.0], np.float32)
+    assert oracle.m1(x) == np.float32(7.875 / 8)
+    assert oracle.m1(np.zeros(0, np.float32)) == 0.0
+
+
+# ---------------------------------------------------------------------------
+# Sign packing and the alternating zero rule
+# ---------------------------------------------------------------------------
+
+def _unpack(words, n):
+    bits = np.unpackbits(np.asarray(words, dtype="<u4").view(np.uint8), bitorder="little")
+    return bits[:n], bits[n:]
+
+
+@pytest.mark.parametrize("n", [1, 31, 32, 33, 1000])
+@pytest.mark.parametrize("t", [0, 1])
+def test_pack_roundtrip_and_tail(oracle_lib, n, t):
+    rng = np.random.default_rng(n * 7 + t)
+    c = rng.standard_normal(n).astype(np.float32)
+    c[:: 5] = 0.0
+    c[1:: 7] = -0.0
+    words = oracle.pack_signs(c, t)
+    assert words.size == (n + 31) // 32
+    bits, tail = _unpack(words, n)
+    want = np.where(c > 0, 1, np.where(c < 0, 0, 1 if t % 2 == 0 else 0))
+    assert bits.tolist() == want.tolist()
+    assert not tail.any()
+
+
+def test_zero_alternates_by_step(oracle_lib):
+    z = np.zeros(32, np.float32)
+    assert oracle.pack_signs(z, 0)[0] == 0xFFFFFFFF
+    assert oracle.pack_signs(z, 1)[0] == 0
+    assert oracle.pack_signs(z, 2)[0] == 0xFFFFFFFF
+    assert oracle.pack_signs(-z, 7)[0] == 0
+    assert oracle.sign_bit(1e-30, 1) == 1 and oracle.sign_bit(-1e-30, 0) == 0
+
+
+def test_zero_rule_closed_form(oracle_lib):
+    """Every worker has g = m = 0, so all bits are the step's zero sign, the vote
+    is +W (even t) or -W (odd t), and theta follows
+    theta_{t+1} = theta_t (1 - lr*wd) -/+ lr."""
+    d, W, lr, wd = 64, 3, 1e-2, 0.1
+    theta = np.linspace(-0.05, 0.05, d).astype(np.float32)
+    th64 = theta.astype(np.float64)
+    m = [np.zeros(d, np.float32) for _ in range(W)]
+    grads = [np.zeros(d, np.uint16) for _ in range(W)]
+    for t in range(8):
+        out = oracle.step(d=d, W=W, layout=None, beta1=0.9, beta2=0.99, lr=lr, wd=wd,
+                          mode=oracle.MODE_SIGN, nbits=1, flags=0, sync_interval=0, t=t,
+                          grads=grads, theta=theta, m=m)
+        s = 1.0 if t % 2 == 0 else -1.0
+        assert all(w.tolist() == ([0xFFFFFFFF] * 2 if s > 0 else [0, 0]) for w in out.wire)
+        assert (out.agg == int(s) * W).all()
+        th64 = th64 - lr * (s + wd * th64)
+        np.testing.assert_allclose(theta, th64, rtol=0, atol=4e-8)
+
+
+# ---------------------------------------------------------------------------
+# Majority vote, integer sums, aggregation rules
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5])
+def test_vote_brute_force(oracle_lib, W):
+    """Bit p of worker i's word is bit i of p, so the 32 positions of one word
+    cover every sign pattern of W <= 5 workers."""
+    words = [np.array([sum(((p >> i) & 1) << p for p in range(32))], np.uint32) for i in range(W)]
+    for p in range(32):
+        if p >= 2 ** W:
+            continue
+        pos = bin(p).count("1")
+        want = pos - (W - pos)
+        assert oracle.vote(words, p) == want
+        want_sign = 1.0 if pos * 2 > W else (-1.0 if pos * 2 < W else 0.0)
+        assert oracle.direction(want, W, 0, 0) == want_sign
+
+
+@pytest.mark.parametrize("W", [1, 2, 7, 16])
+def test_vote_popcount_identity(oracle_lib, W):
+    """sum of +-1 over workers == 2 * popcount - W."""
+    rng = np.random.default_rng(W)
+    words = [rng.integers(0, 2 ** 32, size=4, dtype=np.uint64).astype(np.uint32) for _ in range(W)]
+    bits = np.stack([_unpack(w, 128)[0] for w in words])  # W x 128
+    pop = bits.sum(axis=0)
+    for e in range(128):
+        assert oracle.vote(words, e) == 2 * int(pop[e]) - W
+
+
+@pytest.mark.parametrize("nbits", [2, 4, 8])
+def test_code_sum_brute_force(oracle_lib, nbits):
+    rng = np.random.default_rng(nbits)
+    qmax = 2 ** (nbits - 1) - 1
+    W, n = 6, 77
+    codes = [rng.integers(-qmax, qmax + 1, size=n).astype(np.int8) for _ in range(W)]
+    words = [oracle.pack_codes(q, nbits) for q in codes]
+    total = np.sum(np.stack(codes).astype(np.int64), axis=0)
+    for e in range(n):
+        assert oracle.code_sum(words, nbits, e) == total[e]
+        assert abs(total[e]) <= W * qmax
+
+
+def test_tie_rules(oracle_lib):
+    assert oracle.direction(0, 4, 0, 0) == 0.0
+    assert oracle.direction(0, 4, 0, 1) == 0.0
+    assert oracle.direction(0, 4, oracle.FLAG_TIE_ALTERNATE, 0) == 1.0
+    assert oracle.direction(0, 4, oracle.FLAG_TIE_ALTERNATE, 3) == -1.0
+    assert oracle.direction(2, 4, oracle.FLAG_TIE_ALTERNATE, 1) == 1.0
+
+
+@pytest.mark.parametrize("W", [1, 3, 4, 8])
+def test_average_rule(oracle_lib, W):
+    """D-Lion Avg: the update is the mean of the workers' +-1 signs."""
+    for pos in range(W + 1):
+        agg = 2 * pos - W
+        want = np.float32(Fraction(agg, W).numerator / Fraction(agg, W).denominator)
+        assert oracle.direction(agg, W, oracle.FLAG_AVERAGE, 0) == want
+
+
+def test_apply_closed_forms(oracle_lib):
+    # u = 0: pure decoupled weight decay
+    for th in (0.05, -0.03, 1.0):
+        th = float(np.float32(th))
+        got = oracle.apply(th, 0.0, 1e-4, 0.1)
+        assert abs(got - th * (1 - 1e-5)) <= 2 * abs(float(np.spacing(np.float32(th))))
+    # wd = 0: theta moves by exactly -lr*u
+    assert oracle.apply(0.5, 1.0, 0.25, 0.0) == 0.25
+    assert oracle.apply(0.5, -1.0, 0.25, 0.0) == 0.75
+
+
+# ---------------------------------------------------------------------------
+# W = 1 reduces to textbook Lion
+# ---------------------------------------------------------------------------
+
+def test_single_worker_is_textbook_lion(oracle_lib):
+    """With one worker and no exact-zero update vector, the vote is that worker's
+    sign, so ten steps must equal Lion (Chen et al. 2023) written with
+    np.sign in fp32, bit for bit."""
+    rng = np.random.default_rng(0)
+    d = 4096
+    b1, b2, lr, wd = np.float32(0.9), np.float32(0.99), np.float32(1e-4), np.float32(0.1)
+    theta = rng.uniform(-0.05, 0.05, d).astype(np.float32)
+    m = [np.zeros(d, np.float32)]
+    th_ref, m_ref = theta.copy(), np.zeros(d, np.float32)
+    one = np.float32(1.0)
+    for t in range(10):
+        g = (rng.standard_normal(d) * 1e-3).astype(np.float32)
+        g[g == 0] = np.float32(1e-3)
+        # textbook Lion
+        upd = np.sign(b1 * m_ref + (one - b1) * g).astype(np.float32)
+        assert (upd != 0).all()
+        th_ref = th_ref - lr * (upd + wd * th_ref)
+        m_ref = b2 * m_ref + (one - b2) * g
+        oracle.step(d=d, W=1, layout=None, beta1=float(b1), beta2=float(b2), lr=float(lr),
+                    wd=float(wd), mode=oracle.MODE_SIGN, nbits=1, flags=0, sync_interval=0, t=t,
+                    grads=[g], theta=theta, m=m)
+        assert np.array_equal(theta.view(np.uint32), th_ref.view(np.uint32)), t
+        assert np.array_equal(m[0].view(np.uint32), m_ref.view(np.uint32)), t
+
+
+def test_omega(oracle_lib):
+    assert oracle.omega(0.9) == np.float32(1.0) - np.float32(0.9)
+    assert oracle.omega(0.5) == 0.5
+
+
+# ---------------------------------------------------------------------------
+# Momentum sync and step-level invariants
+# ---------------------------------------------------------------------------
+
+def test_sync_average_against_exact_mean(oracle_lib):
+    rng = np.random.default_rng(11)
+    for W in (1, 2, 3, 16):
+        ms = [rng.standard_normal(300).astype(np.float32) for _ in range(W)]
+        exact = np.mean(np.stack([a.astype(np.float64) for a in ms]), axis=0)
+        bound = np.sum(np.abs(np.stack(ms)).astype(np.float64), axis=0) / W * (W + 1) * 2.0 ** -24
+        oracle.sync_average(ms, 0, 300)
+        for a in ms[1:]:
+            assert np.array_equal(a, ms[0])
+        assert np.all(np.abs(ms[0].astype(np.float64) - exact) <= bound + 1e-45)
+    # power-of-two W with exactly representable sums: exact mean
+    ms = [np.full(4, v, np.float32) for v in (1.0, 2.0, 3.0, 6.0)]
+    oracle.sync_average(ms, 1, 3)
+    assert ms[0].tolist() == [1.0, 3.0, 3.0, 1.0] and ms[3].tolist() == [6.0, 3.0, 3.0, 6.0]
+
+
+def _gpt_like_layout():
+    # three tensors: a flagged "embedding", a middle weight, a ragged last vector
+    return [(0, 320, oracle.TENSOR_SYNC_M), (320, 640, 0), (960, 45, 0)]
+
+
+@pytest.mark.parametrize("mode,nbits", [(oracle.MODE_SIGN, 1), (oracle.MODE_L1, 4), (oracle.MODE_L1, 2)])
+def test_step_invariants(oracle_lib, mode, nbits):
+    rng = np.random.default_rng(3)
+    layout = _gpt_like_layout()
+    d, W = 1005, 4
+    theta = rng.uniform(-0.05, 0.05, d).astype(np.float32)
+    m = [(rng.standard_normal(d) * 1e-3).astype(np.float32) for _ in range(W)]
+    grads = [(rng.standard_t(3.0, d) * 1e-3).astype(np.float32) for _ in range(W)]
+    # a reference run with sync off, for the untouched tensors
+    theta_ns, m_ns = theta.copy(), [a.copy() for a in m]
+    th0 = theta.copy()
+    oracle.step(d=d, W=W, layout=layout, beta1=0.9, beta2=0.99, lr=1e-4, wd=0.1, mode=mode,
+                nbits=nbits, flags=0, sync_interval=0, t=0, grads=grads, theta=theta_ns, m=m_ns)
+    out = oracle.step(d=d, W=W, layout=layout, beta1=0.9, beta2=0.99, lr=1e-4, wd=0.1, mode=mode,
+                      nbits=nbits, flags=0, sync_interval=1, t=0, grads=grads, theta=theta, m=m)
+    assert np.array_equal(theta, theta_ns)  # sync never touches theta
+    for i in range(1, W):
+        assert np.array_equal(m[i][:320], m[0][:320])  # flagged: all workers equal
+    for i in range(W):
+        assert np.array_equal(m[i][320:], m_ns[i][320:])  # unflagged: untouched
+    qmax = 1 if mode == oracle.MODE_SIGN else 2 ** (nbits - 1) - 1
+    assert np.abs(out.agg).max() <= W * qmax
+    if mode == oracle.MODE_SIGN:
+        assert ((out.agg + W) % 2 == 0).all()
+    # padding bits beyond d are zero
+    bits_total = 32 * out.wire[0].size
+    used = d * (1 if mode == oracle.MODE_SIGN else nbits)
+    for w in out.wire:
+        allbits = np.unpackbits(w.view(np.uint8), bitorder="little")
+        assert not allbits[used:bits_total].any()
+    # where the aggregate is zero, theta moved by weight decay only
+    z = out.agg == 0
+    wdonly = np.array([oracle.apply(float(v), 0.0, 1e-4, 0.1) for v in th0[z]], np.float32)
+    assert np.array_equal(theta[z], wdonly)
+    if mode == oracle.MODE_L1:
+        assert out.m1.shape == (W, 3)
+        assert (out.m1 > 0).all()
+
+
+def test_sync_interval(oracle_lib):
+    rng = np.random.default_rng(9)
+    layout = [(0, 64, oracle.TENSOR_SYNC_M)]
+    d, W = 64, 3
+    theta = np.zeros(d, np.float32)
+    m = [np.zeros(d, np.float32) for _ in range(W)]
+    for t in range(6):
+        grads = [rng.standard_normal(d).astype(np.float32) for _ in range(W)]
+        oracle.step(d=d, W=W, layout=layout, beta1=0.9, beta2=0.95, lr=1e-3, wd=0.0,
+                    mode=oracle.MODE_SIGN, nbits=1, flags=0, sync_interval=3, t=t,
+                    grads=grads, theta=theta, m=m)
+        synced = all(np.array_equal(m[0], m[i]) for i in range(W))
+        assert synced == ((t + 1) % 3 == 0), t
+
+
+def test_tie_fraction_statistics(oracle_lib):
+    """At step 0 with m = 0 and i.i.d. symmetric gradients, a tie happens with
+    probability C(W, W/2) / 2^W (37.5% at W=4, 27.3% at W=8, 19.6% at W=16), in
+    line with 'over 30% of the parameters' tied at 4 workers and fewer at 8."""
+    rng = np.random.default_rng(21)
+    d = 20000
+    for W in (4, 8, 16):
+        grads = [(rng.standard_t(3.0, d) * 1e-3).astype(np.float32) for _ in range(W)]
+        theta = np.zeros(d, np.float32)
+        m = [np.zeros(d, np.float32) for _ in range(W)]
+        out = oracle.step(d=d, W=W, layout=None, beta1=0.9, beta2=0.99, lr=1e-4, wd=0.1,
+                          mode=oracle.MODE_SIGN, nbits=1, flags=0, sync_interval=0, t=0,
+                          grads=grads, theta=theta, m=m)
+        p = math.comb(W, W // 2) / 2 ** W
+        frac = float(np.mean(out.agg == 0))
+        assert abs(frac - p) < 5 * math.sqrt(p * (1 - p) / d), (W, frac, p)
+
+
+def test_step_rejects_bad_arguments(oracle_lib):
+    d = 40
+    g = [np.zeros(d, np.float32)]
+    m = [np.zeros(d, np.float32)]
+    th = np.zeros(d, np.float32)
+    kw = dict(d=d, W=1, beta1=0.9, beta2=0.99, lr=1e-4, wd=0.1, flags=0, sync_interval=0, t=0,
+              grads=g, theta=th, m=m)
+    with pytest.raises(ValueError):
+        oracle.step(layout=[(0, 20, 0), (20, 20, 0)], mode=0, nbits=1, **kw)  # offset not 32-aligned
+    with pytest.raises(ValueError):
+        oracle.step(layout=[(0, 32, 0)], mode=0, nbits=1, **kw)  # does not cover d
+    with pytest.raises(ValueError):
+        oracle.step(layout=None, mode=1, nbits=3, **kw)
