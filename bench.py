@@ -1,0 +1,467 @@
+"""Benchmark of the compressed Lion update step (Lion Cub / Distributed Lion)
+with W simulated workers on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl lioncub|reference]
+
+One step = one pass of the whole path over one batch of synthetic gradients:
+update vectors, compression (packed signs or L1 codes, with the M1 pass),
+the W-way vote or integer sum, the global sign and the theta update, the
+momentum update and the selective momentum sync.  The default workload is
+GPT-2 small (124,439,808 parameters), W = 8 workers, bf16 gradients
+1e-3 * Student-t(3), 1-bit signs with majority vote.
+
+Metric: parameter-elements per second per step (d / step time), whole job.
+Inputs are far larger than the 129 MB L2 for every GPT workload (11-200 GB
+moved per step); the 1M-element workload flushes L2 between timed steps.
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the path exchanges nothing between GPUs on one
+box), the timed region is bracketed by barriers, and the step time is the
+maximum over ranks.  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+DEFAULT_CONFIG = 2
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (every byte that must move, per parameter)
+# ---------------------------------------------------------------------------
+
+def kernel_bytes(wl: synth.Workload) -> dict:
+    """Algorithmic bytes per step of each kernel for workload wl."""
+    d, W = wl.d, wl.W
+    G = 4 if wl.grad == "f32" else 2
+    bits = wl.nbits if wl.mode == 1 else 1
+    out = {"compress": d * W * (G + 4 + 4) + W * ((d * bits + 31) // 32) * 4,
+           "reduce_apply": W * ((d * bits + 31) // 32) * 4 + 8 * d}
+    if wl.mode == 1:
+        out["m1_partial"] = d * W * (G + 4)
+        out["m1_finalize"] = 0
+    return out
+
+
+def step_bytes(wl: synth.Workload) -> int:
+    return sum(kernel_bytes(wl).values())
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; only the timing is reduced)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = json.load(f)
+        return float(v["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl: synth.Workload, target_elems: int):
+    """A sample of the workload: its tensors in layout order (after the two
+    embeddings, which would dominate), the last one cut so that the sample
+    holds about target_elems elements."""
+    body = [t for t in wl.layout if t[0] not in ("wte", "wpe", "head")] or wl.layout
+    sub, names, dst = [], [], 0
+    for (name, off, n, fl) in body:
+        if dst >= target_elems:
+            break
+        take = min(n, target_elems - dst)
+        if take < n:
+            take = max(32, take // 32 * 32)
+        sub.append((dst, take, fl))
+        names.append(name)
+        dst += take
+    return sub, dst, names
+
+
+def time_oracle_steps(wl: synth.Workload, target_elems: int, steps: int, warmup: int = 0):
+    import oracle
+    sub, dsub, names = oracle_sample(wl, target_elems)
+    grads_pool = [synth.numpy_grad(wl, dsub, 0, i) for i in range(min(wl.W, 2))]
+    grads = [np.roll(grads_pool[i % len(grads_pool)], 977 * i) for i in range(wl.W)]
+    theta = synth.numpy_theta(wl, dsub)
+    m = [np.zeros(dsub, np.float32) for _ in range(wl.W)]
+    times = []
+    for t in range(warmup + steps):
+        t0 = time.perf_counter()
+        oracle.step(d=dsub, W=wl.W, layout=sub, beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr, wd=wl.wd,
+                    mode=wl.mode, nbits=wl.nbits, flags=0, sync_interval=wl.sync_interval, t=t,
+                    grads=grads, theta=theta, m=m, want_outputs=False)
+        if t >= warmup:
+            times.append(time.perf_counter() - t0)
+    return dsub, names, times
+
+
+def oracle_rate_probe(wl: synth.Workload) -> float:
+    """Seconds per parameter of one oracle step (small probe)."""
+    dsub, _, times = time_oracle_steps(wl, 300_000, 1)
+    return times[0] / dsub
+
+
+def cpu_info():
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                low = line.lower()
+                if low.startswith("model name") or low.startswith("cpu part"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cores": os.cpu_count(), "cpu": model}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, wl: synth.Workload):
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    from communication_compressed_sign_gb300 import lioncub as lc
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(dev)
+    lc.load()
+
+    d, W = wl.d, wl.W
+    gdt = synth.grad_dtype(wl)
+    theta = torch.empty(d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+    nsets = 2
+    grads = [[torch.empty(d, dtype=gdt, device=dev) for _ in range(W)] for _ in range(nsets)]
+    for s in range(nsets):
+        for i in range(W):
+            synth.fill_grad_(grads[s][i], wl, s, i)
+    gptrs = [[g.data_ptr() for g in grads[s]] for s in range(nsets)]
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd, wl.mode,
+                          wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16, wl.sync_interval)
+    lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ws_bytes = step_bytes(wl)
+    flush = ws_bytes < 4 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    launches_per_step = 4 if wl.mode == 1 else 2
+
+    # warm-up
+    for s in range(args.warmup):
+        lc.lioncub_step(h, gptrs[s % nsets], sp)
+    torch.cuda.synchronize(dev)
+
+    # timed region: per-kernel events inside the library, step events here
+    lc.lioncub_profile(h, args.steps)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    if flush:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for s in range(args.steps):
+            flush_buf.fill_(float(s))
+            ev[s][0].record(stream)
+            lc.lioncub_step(h, gptrs[s % nsets], sp)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            lc.lioncub_step(h, gptrs[s % nsets], sp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = e0.elapsed_time(e1)
+    barrier(dev)
+    clk = clocks.stop()
+    ms_local = total_ms / args.steps
+    ms = reduce_max(ms_local, dev)
+
+    kb = kernel_bytes(wl)
+    per_kernel = {}
+    for k, name in lc.KERNEL_NAMES.items():
+        tot, n = lc.lioncub_profile_read(h, k)
+        if n:
+            per_kernel[name] = {"ms_avg": tot / n, "launches": n, "share": None,
+                                "alg_bytes": kb.get(name, 0)}
+    ksum = sum(v["ms_avg"] for v in per_kernel.values()) or 1.0
+    for v in per_kernel.values():
+        v["share"] = v["ms_avg"] / ksum
+    lc.lioncub_profile(h, 0)
+    top = max(per_kernel, key=lambda k: per_kernel[k]["ms_avg"])
+    peak, peak_kind = measured_hbm_peak()
+    achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_avg"] * 1e-3) / 1e9
+    step_gbs = ws_bytes / (ms * 1e-3) / 1e9
+
+    # end to end: host gradients in, host theta out, through lioncub_step_host
+    e2e = run_e2e(args, wl, h, dev, stream)
+
+    lc.lioncub_destroy(h)
+    del grads, m, theta, flush_buf
+    torch.cuda.empty_cache()
+
+    result = {
+        "metric": "param-elements/s per Lion Cub step (W simulated workers)",
+        "value": ws * d / (ms * 1e-3),
+        "unit": "param-elements/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": f"{'bf16' if wl.grad == 'bf16' else 'f32'} grads, f32 theta/m, u32 wire",
+        "data": "synthetic (seeded counter-based Student-t / normal gradients, uniform theta)",
+        "config": {
+            "workload": wl.name,
+            "workers": W,
+            "params": d,
+            "tensors": len(wl.layout),
+            "mode": "sign+majority" if wl.mode == 0 else f"L1 n={wl.nbits} + int sum",
+            "grad_dtype": wl.grad,
+            "sync": "wte every step" if wl.sync_interval else "none",
+            "parallelism": f"replicas x{ws} (no inter-GPU exchange)",
+            "l2": "flushed between timed steps" if flush else f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB moved per step)",
+        },
+        "hbm": {"alg_bytes_per_step": ws_bytes, "achieved_gbs": step_gbs, "peak_gbs": peak,
+                "frac_of_measured" if peak_kind == "measured" else "frac_of_fallback": step_gbs / peak,
+                "frac_of_nominal_7900": step_gbs / 7900.0},
+        "roofline": {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": None},
+        "kernels": per_kernel,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    if ws > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def run_e2e(args, wl, h, dev, stream):
+    """K steps through lioncub_step_host: every step copies the W gradient
+    buffers from pinned host memory to the device and theta back."""
+    import torch
+    from communication_compressed_sign_gb300 import lioncub as lc
+    d, W = wl.d, wl.W
+    gdt = synth.grad_dtype(wl)
+    host = [[torch.empty(d, dtype=gdt).pin_memory() for _ in range(W)] for _ in range(2)]
+    tmp = torch.empty(d, dtype=gdt, device=dev)
+    for s in range(2):
+        for i in range(W):
+            synth.fill_grad_(tmp, wl, s, i)
+            host[s][i].copy_(tmp)
+    del tmp
+    theta_host = torch.empty(d, dtype=torch.float32).pin_memory()
+    ptrs = [[x.data_ptr() for x in host[s]] for s in range(2)]
+    sp = stream.cuda_stream
+    for s in range(max(1, args.warmup)):
+        lc.lioncub_step_host(h, ptrs[s % 2], theta_host.data_ptr(), sp)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        lc.lioncub_step_host(h, ptrs[s % 2], theta_host.data_ptr(), sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, dev)
+    ws, _, _ = dist_env()
+    G = 4 if wl.grad == "f32" else 2
+    return {"value": ws * d / (ms * 1e-3), "unit": "param-elements/s", "ms_per_step": ms,
+            "wall_ms_per_step": wall * 1e3 / args.steps,
+            "h2d_bytes_per_step": W * d * G, "d2h_bytes_per_step": 4 * d,
+            "api": "lioncub_step_host (pinned host buffers)"}
+
+
+def cpu_baseline(wl: synth.Workload, seconds: float = 12.0):
+    rate = oracle_rate_probe(wl)
+    target = int(min(wl.d, max(100_000, seconds / max(rate, 1e-12))))
+    dsub, names, times = time_oracle_steps(wl, target, 1)
+    info = cpu_info()
+    return {"value": dsub / times[0], "unit": "param-elements/s", "cores": 1, "kind": "oracle",
+            "sample": f"one step of {wl.name} restricted to {len(names)} whole tensors "
+                      f"({dsub} of {wl.d} params, all {wl.W} workers), numpy-generated inputs "
+                      f"of the same distribution",
+            "seconds": times[0], **info}
+
+
+def run_reference(args, wl: synth.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    rate = oracle_rate_probe(wl)
+    budget_s = 150.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    target = int(min(wl.d, max(50_000, per_step / max(rate, 1e-12))))
+    dsub, names, times = time_oracle_steps(wl, target, args.steps, args.warmup)
+    ms = 1e3 * sum(times) / len(times)
+    value = dsub / (ms * 1e-3)
+    info = cpu_info()
+    return {
+        "impl": "reference",
+        "metric": "param-elements/s per Lion Cub step (W simulated workers)",
+        "value": value,
+        "unit": "param-elements/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (CPU oracle), bf16 grads" if wl.grad == "bf16" else "f32 (CPU oracle)",
+        "data": "synthetic (numpy Student-t / normal gradients of the workload's distribution)",
+        "config": {"workload": wl.name, "workers": wl.W, "params": wl.d,
+                   "sample_params": dsub, "sample_tensors": len(names)},
+        "cpu_baseline": {"value": value, "unit": "param-elements/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(names)} whole tensors, {dsub} of {wl.d} params, all workers",
+                         **info},
+        "e2e": {"value": value, "unit": "param-elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(synth.workloads()))
+    ap.add_argument("--impl", default="lioncub", choices=["lioncub", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "lioncub":
+        print("note: warm-up raised to 3 steps", file=sys.stderr)
+        args.warmup = 3
+    wl = synth.workloads()[args.config]
+    res = run_reference(args, wl) if args.impl == "reference" else run_gpu(args, wl)
+    if res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+// compress.cu -- per-worker compression pass of the compressed Lion step.
+//
+// One block per tile (2048 elements of one tensor), 8 consecutive elements
+// per thread.  For each worker i in turn the thread loads 8 gradients and 8
+// momenta, forms the update vector c ("Lion Cub: Minimizing Communication
+// Overhead in Distributed Lion", "What carries the argument"), emits the
+// wire bits -- a 0/1 sign with exact zeros sent as the step's alternating
+// sign, or the Eq. (1) L1 code -- and writes the worker's new momentum.  On
+// tensors whose momentum is synchronized this step the new momenta are
+// summed in worker order in registers and the mean is written to every
+// worker instead, so the sync costs no extra pass over memory.
+//
+// Wire packing (LSB first): a thread's 8 elements hold 8*NB bits.  For the
+// 1-bit sign, four neighbouring lanes' bytes form one 32-bit word; for 2-bit
+// codes two lanes' halves; 4-bit codes fill one word per thread; 8-bit codes
+// two words.
+#include "device_common.cuh"
+
+namespace lc {
+namespace {
+
+// Sign bit of the transmitted update: 1 = +1, 0 = -1, exact zero = zero_bit.
+__device__ __forceinline__ uint32_t sign_bit(float c, uint32_t zero_bit)
+{
+    return c > 0.0f ? 1u : (c < 0.0f ? 0u : zero_bit);
+}
+
+// Eq. (1) code of c with the per-(worker, tensor) scale inv = RN(qmax / M1):
+// round half to even, a NaN product reads as 0, clamp to [-qmax, qmax].
+__device__ __forceinline__ int q1_code(float c, float inv, float qmax)
+{
+    if (inv == 0.0f)
+        return 0;  // M1 == 0: the whole tensor is zero
+    float r = rintf(__fmul_rn(c, inv));
+    if (r != r)
+        r = 0.0f;
+    r = fminf(fmaxf(r, -qmax), qmax);
+    return static_cast<int>(r);
+}
+
+// Write this thread's 8*NB wire bits (in `bits`, low bits first) of the tile
+// element group starting at e0 into the worker's wire words.
+template <int NB>
+__device__ __forceinline__ void store_wire(uint32_t* wire_i, int64_t e0, int valid, uint64_t bits)
+{
+    const int lane = threadIdx.x & 31;
+    if constexpr (NB == 1) {
+        const uint32_t b = static_cast<uint32_t>(bits);
+        const uint32_t w = b | (__shfl_down_sync(0xffffffffu, b, 1) << 8) |
+                           (__shfl_down_sync(0xffffffffu, b, 2) << 16) |
+                           (__shfl_down_sync(0xffffffffu, b, 3) << 24);
+        if ((lane & 3) == 0 && valid > 0)
+            __stcg(wire_i + (e0 >> 5), w);
+    } else if constexpr (NB == 2) {
+        const uint32_t h = static_cast<uint32_t>(bits);
+        const uint32_t w = h | (__shfl_down_sync(0xffffffffu, h, 1) << 16);
+        if ((lane & 1) == 0 && valid > 0)
+            __stcg(wire_i + (e0 >> 4), w);
+    } else if constexpr (NB == 4) {
+        if (valid > 0)
+            __stcg(wire_i + (e0 >> 3), static_cast<uint32_t>(bits));
+    } else {
+        if (valid > 0)
+            __stcg(reinterpret_cast<uint2*>(wire_i + (e0 >> 2)),
+                   make_uint2(static_cast<uint32_t>(bits), static_cast<uint32_t>(bits >> 32)));
+    }
+}
+
+template <typename GT, int NB>
+__global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a)
+{
+    const Tile tl = a.tiles[blockIdx.x];
+    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    const bool sync = a.sync_now && (tl.meta & kTileSync);
+    const int k = static_cast<int>(tl.meta & ~kTileSync);
+    const uint64_t fmask = (NB == 8) ? 0xffull : ((1ull << NB) - 1ull);
+
+    float acc[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j)
+        acc[j] = 0.0f;
+
+    for (int i = 0; i < a.W; ++i) {
+        float g[kVec], m[kVec];
+        if (valid > 0) {
+            load_grad<GT>(a.g[i], e0, valid, g);
+            load_f32(a.m[i], e0, valid, m);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                g[j] = m[j] = 0.0f;
+        }
+        float inv = 0.0f;
+        if constexpr (NB > 1)
+            inv = a.inv[static_cast<int64_t>(i) * a.K + k];
+
+        uint64_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
+            uint64_t field;
+            if constexpr (NB == 1)
+                field = sign_bit(c, a.zero_bit);
+            else
+                field = static_cast<uint64_t>(static_cast<uint32_t>(q1_code(c, inv, a.qmax))) & fmask;
+            if (j < valid)
+                bits |= field << (NB * j);
+            m[j] = momentum(m[j], g[j], a.beta2, a.omega2);
+        }
+        store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
+
+        if (sync) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
+        } else if (valid > 0) {
+            store_f32(a.m[i], e0, valid, m);
+        }
+    }
+
+    if (sync && valid > 0) {
+        const float fw = static_cast<float>(a.W);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            acc[j] = __fdiv_rn(acc[j], fw);
+        for (int i = 0; i < a.W; ++i)
+            store_f32(a.m[i], e0, valid, acc);
+    }
+}
+
+template <typename GT>
+cudaError_t launch_typed(const StepArgs& a, int nb, cudaStream_t s)
+{
+    const dim3 grid(static_cast<unsigned>(a.ntiles)), block(kThreads);
+    switch (nb) {
+    case 1: k_compress<GT, 1><<<grid, block, 0, s>>>(a); break;
+    case 2: k_compress<GT, 2><<<grid, block, 0, s>>>(a); break;
+    case 4: k_compress<GT, 4><<<grid, block, 0, s>>>(a); break;
+    case 8: k_compress<GT, 8><<<grid, block, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s)
+{
+    if (a.ntiles == 0)
+        return cudaSuccess;
+    const int nb = l1_mode ? a.nbits : 1;
+    if (grad_dtype == LIONCUB_GRAD_BF16)
+        return launch_typed<__nv_bfloat16>(a, nb, s);
+    return launch_typed<float>(a, nb, s);
+}
+
+}  // namespace lc

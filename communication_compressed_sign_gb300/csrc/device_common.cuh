@@ -1,0 +1,145 @@
+// device_common.cuh -- element loads/stores and the per-element arithmetic
+// shared by the compress and M1 kernels.
+//
+// Every float operation is an explicit round-to-nearest intrinsic
+// (__fmul_rn / __fadd_rn / __fdiv_rn), which the compiler never contracts
+// into a fused multiply-add, so each product and sum rounds once.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace lc {
+
+// --- gradient loads: 8 consecutive elements -> 8 floats ---------------------
+// Gradients and momenta are read once per step, so loads use the streaming
+// (evict-first) cache hint and leave L2 to the small wire buffer.
+
+__device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename GT>
+struct GradIO;
+
+template <>
+struct GradIO<__nv_bfloat16> {
+    __device__ __forceinline__ static void load8(const void* base, int64_t e0, float* g)
+    {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e0));
+        g[0] = bf16_bits_lo(v.x); g[1] = bf16_bits_hi(v.x);
+        g[2] = bf16_bits_lo(v.y); g[3] = bf16_bits_hi(v.y);
+        g[4] = bf16_bits_lo(v.z); g[5] = bf16_bits_hi(v.z);
+        g[6] = bf16_bits_lo(v.w); g[7] = bf16_bits_hi(v.w);
+    }
+    __device__ __forceinline__ static float load1(const void* base, int64_t e)
+    {
+        return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(base)[e]) << 16);
+    }
+};
+
+template <>
+struct GradIO<float> {
+    __device__ __forceinline__ static void load8(const void* base, int64_t e0, float* g)
+    {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e0);
+        const float4 a = __ldcs(p);
+        const float4 b = __ldcs(p + 1);
+        g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+        g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+    }
+    __device__ __forceinline__ static float load1(const void* base, int64_t e)
+    {
+        return static_cast<const float*>(base)[e];
+    }
+};
+
+// Load `valid` (0..8) elements starting at e0; the rest read as 0.
+template <typename GT>
+__device__ __forceinline__ void load_grad(const void* base, int64_t e0, int valid, float* g)
+{
+    if (valid == kVec) {
+        GradIO<GT>::load8(base, e0, g);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            g[j] = (j < valid) ? GradIO<GT>::load1(base, e0 + j) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void load_f32(const float* base, int64_t e0, int valid, float* x)
+{
+    if (valid == kVec) {
+        const float4* p = reinterpret_cast<const float4*>(base + e0);
+        const float4 a = __ldcs(p);
+        const float4 b = __ldcs(p + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            x[j] = (j < valid) ? base[e0 + j] : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void store_f32(float* base, int64_t e0, int valid, const float* x)
+{
+    if (valid == kVec) {
+        float4* p = reinterpret_cast<float4*>(base + e0);
+        __stcs(p, make_float4(x[0], x[1], x[2], x[3]));
+        __stcs(p + 1, make_float4(x[4], x[5], x[6], x[7]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            if (j < valid)
+                base[e0 + j] = x[j];
+    }
+}
+
+// --- the method's per-element arithmetic ------------------------------------
+
+// Update vector of one worker ("What carries the argument"):
+// c = beta1 * m + (1 - beta1) * g, with omega1 = RN(1 - beta1) from the host.
+__device__ __forceinline__ float update_vector(float m, float g, float beta1, float omega1)
+{
+    return __fadd_rn(__fmul_rn(beta1, m), __fmul_rn(omega1, g));
+}
+
+// Per-worker Lion momentum: m' = beta2 * m + (1 - beta2) * g.
+__device__ __forceinline__ float momentum(float m, float g, float beta2, float omega2)
+{
+    return __fadd_rn(__fmul_rn(beta2, m), __fmul_rn(omega2, g));
+}
+
+// Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Compensated accumulator (hi, lo): add x.
+__device__ __forceinline__ void cacc_add(float& hi, float& lo, float x)
+{
+    float s, e;
+    two_sum(hi, x, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// Combine two compensated accumulators.
+__device__ __forceinline__ void cacc_merge(float& hi, float& lo, float ohi, float olo)
+{
+    float s, e;
+    two_sum(hi, ohi, s, e);
+    e = __fadd_rn(e, __fadd_rn(lo, olo));
+    // renormalise so that |lo| stays below half an ulp of hi
+    const float h = __fadd_rn(s, e);
+    lo = __fsub_rn(e, __fsub_rn(h, s));
+    hi = h;
+}
+
+}  // namespace lc

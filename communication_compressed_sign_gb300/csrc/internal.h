@@ -1,0 +1,61 @@
+// internal.h -- shared declarations of the lioncub CUDA library (not part of
+// the public C ABI in include/lioncub.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lioncub.h"
+
+namespace lc {
+
+// Tiled kernels: 256 threads, 8 consecutive elements per thread, so one tile
+// is 2048 elements.  Tiles never cross a tensor boundary (tensor offsets are
+// multiples of 32 elements), which keeps every packed word inside one tile
+// and gives each tile one tensor's M1 scale.
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+constexpr int kTile = kThreads * kVec;
+
+// One tile: elements [start, start + len); meta = tensor index, with bit 31
+// set when the tensor's momentum is synchronized across workers.
+struct Tile {
+    int64_t start;
+    int32_t len;
+    uint32_t meta;
+};
+constexpr uint32_t kTileSync = 0x80000000u;
+
+// Everything a step's kernels read, passed by value (about 2.2 KB).
+struct StepArgs {
+    const void* g[LIONCUB_MAX_WORKERS];
+    float* m[LIONCUB_MAX_WORKERS];
+    float* theta;
+    uint32_t* wire;         // W x wire_stride words (packed signs or codes)
+    int64_t wire_stride;    // words per worker, a multiple of 4
+    int64_t d;
+    const Tile* tiles;
+    int64_t ntiles;
+    const int32_t* tile_first;  // K + 1 entries: tiles of tensor k are [tile_first[k], tile_first[k+1])
+    const int64_t* numel;       // K entries
+    float2* partials;           // W x ntiles compensated (hi, lo) sums of |c| (L1 mode)
+    float* m1;                  // W x K (L1 mode)
+    float* inv;                 // W x K: RN(qmax / M1), 0 where M1 == 0 (L1 mode)
+    int W;
+    int K;
+    int nbits;
+    float beta1, omega1, beta2, omega2, lr, wd, qmax;
+    uint32_t zero_bit;  // the bit an exact zero is sent as: 1 on even steps, 0 on odd
+    int sync_now;       // 1 when flagged tensors average their momentum this step
+    int average;        // 1: u = agg / W (D-Lion Avg)
+    float tie_u;        // u for agg == 0: 0, or the step's zero sign
+};
+
+// Kernel launchers (return the launch status).
+cudaError_t launch_compress(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s);
+cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s);
+cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s);
+cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s);
+
+}  // namespace lc

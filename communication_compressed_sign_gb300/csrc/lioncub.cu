@@ -1,0 +1,567 @@
+// lioncub.cu -- the C ABI (include/lioncub.h): handle life cycle, layout
+// validation, scratch ownership, step sequencing and error reporting.
+//
+// A step is two launches in sign mode (compress, reduce_apply) and four in
+// L1 mode (m1_partial, m1_finalize, compress, reduce_apply), all on the
+// caller's stream with no host synchronization.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using lc::StepArgs;
+using lc::Tile;
+
+struct lioncub_s {
+    int device = 0;
+    int64_t d = 0;
+    int W = 0;
+    int K = 0;
+    int mode = 0;        // LIONCUB_MODE_*
+    uint32_t flags = 0;  // LIONCUB_FLAG_*
+    int nbits = 1;
+    int grad_dtype = 0;
+    int sync_interval = 0;
+    float beta1 = 0, beta2 = 0, lr = 0, wd = 0;
+    int64_t t = 0;
+    bool bound = false;
+    float* theta = nullptr;
+    float* m[LIONCUB_MAX_WORKERS] = {};
+
+    std::vector<lioncub_tensor> layout;
+    int64_t ntiles = 0;
+    int64_t wire_words = 0;   // per worker, dense
+    int64_t wire_stride = 0;  // per worker, padded to 4 words
+
+    // device scratch owned by the library
+    uint32_t* wire = nullptr;
+    Tile* tiles = nullptr;
+    int32_t* tile_first = nullptr;
+    int64_t* numel = nullptr;
+    float2* partials = nullptr;
+    float* m1 = nullptr;
+    float* inv = nullptr;
+    // staging for lioncub_step_host
+    void* staging = nullptr;
+
+    // profiling
+    int prof_capacity = 0;  // launches that can still be recorded
+    std::vector<cudaEvent_t> prof_events;  // pairs
+    std::vector<int> prof_kernel;
+    int prof_used = 0;
+
+    std::string err;
+};
+
+namespace {
+
+// Message of the last failed lioncub_create on this thread (no handle exists
+// to hold it).
+thread_local std::string g_create_err;
+
+int fail(lioncub_t h, int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (h)
+        h->err = buf;
+    else
+        g_create_err = buf;
+    return code;
+}
+
+int cuda_fail(lioncub_t h, cudaError_t e, const char* what)
+{
+    return fail(h, LIONCUB_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_scratch(lioncub_t h)
+{
+    void* ptrs[] = {h->wire, h->tiles, h->tile_first, h->numel, h->partials, h->m1, h->inv, h->staging};
+    for (void* p : ptrs)
+        if (p)
+            cudaFree(p);
+    h->wire = nullptr;
+    h->tiles = nullptr;
+    h->tile_first = nullptr;
+    h->numel = nullptr;
+    h->partials = nullptr;
+    h->m1 = h->inv = nullptr;
+    h->staging = nullptr;
+}
+
+void drop_profile(lioncub_t h)
+{
+    for (cudaEvent_t e : h->prof_events)
+        cudaEventDestroy(e);
+    h->prof_events.clear();
+    h->prof_kernel.clear();
+    h->prof_capacity = 0;
+    h->prof_used = 0;
+}
+
+template <typename T>
+cudaError_t dev_alloc(T** p, size_t count)
+{
+    *p = nullptr;
+    if (count == 0)
+        count = 1;
+    return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+StepArgs make_args(lioncub_t h, const void* const* grads)
+{
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int i = 0; i < h->W; ++i) {
+        a.g[i] = grads ? grads[i] : nullptr;
+        a.m[i] = h->m[i];
+    }
+    a.theta = h->theta;
+    a.wire = h->wire;
+    a.wire_stride = h->wire_stride;
+    a.d = h->d;
+    a.tiles = h->tiles;
+    a.ntiles = h->ntiles;
+    a.tile_first = h->tile_first;
+    a.numel = h->numel;
+    a.partials = h->partials;
+    a.m1 = h->m1;
+    a.inv = h->inv;
+    a.W = h->W;
+    a.K = h->K;
+    a.nbits = h->nbits;
+    a.beta1 = h->beta1;
+    a.omega1 = 1.0f - h->beta1;  // one fp32 rounding, on the host
+    a.beta2 = h->beta2;
+    a.omega2 = 1.0f - h->beta2;
+    a.lr = h->lr;
+    a.wd = h->wd;
+    a.qmax = static_cast<float>((1 << (h->nbits - 1)) - 1);
+    const bool even = (h->t % 2) == 0;
+    a.zero_bit = even ? 1u : 0u;
+    a.sync_now = (h->sync_interval > 0 && (h->t + 1) % h->sync_interval == 0) ? 1 : 0;
+    a.average = (h->flags & LIONCUB_FLAG_AVERAGE) ? 1 : 0;
+    a.tie_u = (h->flags & LIONCUB_FLAG_TIE_ALTERNATE) ? (even ? 1.0f : -1.0f) : 0.0f;
+    return a;
+}
+
+// Records an event before a launch when profiling is on; returns the slot.
+int prof_begin(lioncub_t h, int kernel, cudaStream_t s)
+{
+    if (h->prof_used >= h->prof_capacity)
+        return -1;
+    const int slot = h->prof_used++;
+    h->prof_kernel[slot] = kernel;
+    cudaEventRecord(h->prof_events[2 * slot], s);
+    return slot;
+}
+
+void prof_end(lioncub_t h, int slot, cudaStream_t s)
+{
+    if (slot >= 0)
+        cudaEventRecord(h->prof_events[2 * slot + 1], s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lioncub_strerror(int code)
+{
+    switch (code) {
+    case LIONCUB_OK: return "LIONCUB_OK";
+    case LIONCUB_ERR_ARG: return "LIONCUB_ERR_ARG";
+    case LIONCUB_ERR_ALIGN: return "LIONCUB_ERR_ALIGN";
+    case LIONCUB_ERR_STATE: return "LIONCUB_ERR_STATE";
+    case LIONCUB_ERR_OOM: return "LIONCUB_ERR_OOM";
+    case LIONCUB_ERR_CUDA: return "LIONCUB_ERR_CUDA";
+    default: return "LIONCUB_ERR_UNKNOWN";
+    }
+}
+
+const char* lioncub_last_error(lioncub_t h)
+{
+    return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layout, int K,
+                   float beta1, float beta2, float lr, float wd, int mode, int nbits,
+                   int grad_dtype, int sync_interval)
+{
+    if (!out)
+        return LIONCUB_ERR_ARG;
+    *out = nullptr;
+    lioncub_s* h = new (std::nothrow) lioncub_s();
+    if (!h)
+        return LIONCUB_ERR_OOM;
+
+    const int base_mode = mode & 0xff;
+    const uint32_t flags = static_cast<uint32_t>(mode) & ~0xffu;
+    int rc = LIONCUB_OK;
+    if (d < 0 || W < 1 || W > LIONCUB_MAX_WORKERS || K < 0 || (K > 0 && !layout))
+        rc = fail(h, LIONCUB_ERR_ARG, "bad sizes: d=%lld W=%d K=%d", (long long)d, W, K);
+    else if (base_mode != LIONCUB_MODE_SIGN_MAJORITY && base_mode != LIONCUB_MODE_L1_INTSUM)
+        rc = fail(h, LIONCUB_ERR_ARG, "unknown mode %d", base_mode);
+    else if (flags & ~static_cast<uint32_t>(LIONCUB_FLAG_TIE_ALTERNATE | LIONCUB_FLAG_AVERAGE))
+        rc = fail(h, LIONCUB_ERR_ARG, "unknown mode flags 0x%x", flags);
+    else if ((flags & LIONCUB_FLAG_AVERAGE) &&
+             (base_mode != LIONCUB_MODE_SIGN_MAJORITY || (flags & LIONCUB_FLAG_TIE_ALTERNATE)))
+        rc = fail(h, LIONCUB_ERR_ARG, "the average rule applies to sign mode only, without tie alternation");
+    else if (base_mode == LIONCUB_MODE_L1_INTSUM && nbits != 2 && nbits != 4 && nbits != 8)
+        rc = fail(h, LIONCUB_ERR_ARG, "nbits must be 2, 4 or 8 in L1 mode (got %d)", nbits);
+    else if (grad_dtype != LIONCUB_GRAD_BF16 && grad_dtype != LIONCUB_GRAD_F32)
+        rc = fail(h, LIONCUB_ERR_ARG, "unknown gradient dtype %d", grad_dtype);
+    else if (sync_interval < 0)
+        rc = fail(h, LIONCUB_ERR_ARG, "sync_interval must be >= 0");
+    if (rc != LIONCUB_OK) {
+        g_create_err = h->err;
+        delete h;
+        return rc;
+    }
+    g_create_err.clear();
+
+    h->d = d;
+    h->W = W;
+    h->mode = base_mode;
+    h->flags = flags;
+    h->nbits = base_mode == LIONCUB_MODE_SIGN_MAJORITY ? 1 : nbits;
+    h->grad_dtype = grad_dtype;
+    h->sync_interval = sync_interval;
+    h->beta1 = beta1;
+    h->beta2 = beta2;
+    h->lr = lr;
+    h->wd = wd;
+    if (K == 0) {
+        h->layout.push_back(lioncub_tensor{0, d, 0u});
+    } else {
+        h->layout.assign(layout, layout + K);
+    }
+    h->K = static_cast<int>(h->layout.size());
+
+    // Validate: tensors tile [0, d) in order, 32-aligned offsets.
+    int64_t next = 0;
+    for (int k = 0; k < h->K; ++k) {
+        const lioncub_tensor& T = h->layout[k];
+        if (T.offset % 32 != 0) {
+            rc = fail(h, LIONCUB_ERR_ALIGN, "tensor %d offset %lld is not a multiple of 32", k, (long long)T.offset);
+            break;
+        }
+        if (T.offset != next || T.numel < 0) {
+            rc = fail(h, LIONCUB_ERR_ARG, "tensor %d [%lld, +%lld) does not continue the layout at %lld", k,
+                      (long long)T.offset, (long long)T.numel, (long long)next);
+            break;
+        }
+        if (T.flags & ~static_cast<uint32_t>(LIONCUB_TENSOR_SYNC_M)) {
+            rc = fail(h, LIONCUB_ERR_ARG, "tensor %d has unknown flags 0x%x", k, T.flags);
+            break;
+        }
+        next += T.numel;
+    }
+    if (rc == LIONCUB_OK && next != d)
+        rc = fail(h, LIONCUB_ERR_ARG, "layout covers %lld elements, d is %lld", (long long)next, (long long)d);
+    if (rc != LIONCUB_OK) {
+        g_create_err = h->err;
+        delete h;
+        return rc;
+    }
+
+    // Tile table.
+    std::vector<Tile> tiles;
+    std::vector<int32_t> first(h->K + 1, 0);
+    std::vector<int64_t> numel(h->K, 0);
+    for (int k = 0; k < h->K; ++k) {
+        const lioncub_tensor& T = h->layout[k];
+        first[k] = static_cast<int32_t>(tiles.size());
+        numel[k] = T.numel;
+        const uint32_t meta = static_cast<uint32_t>(k) | ((T.flags & LIONCUB_TENSOR_SYNC_M) ? lc::kTileSync : 0u);
+        for (int64_t s = 0; s < T.numel; s += lc::kTile) {
+            const int64_t len = (T.numel - s) < lc::kTile ? (T.numel - s) : lc::kTile;
+            tiles.push_back(Tile{T.offset + s, static_cast<int32_t>(len), meta});
+        }
+        if (tiles.size() > 0x7fffffffu) {
+            delete h;
+            return fail(nullptr, LIONCUB_ERR_ARG, "too many tiles");
+        }
+    }
+    first[h->K] = static_cast<int32_t>(tiles.size());
+    h->ntiles = static_cast<int64_t>(tiles.size());
+    h->wire_words = (d * h->nbits + 31) / 32;
+    h->wire_stride = (h->wire_words + 3) / 4 * 4;
+
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = dev_alloc(&h->wire, static_cast<size_t>(W) * h->wire_stride + 4);
+    if (e == cudaSuccess) e = dev_alloc(&h->tiles, tiles.size());
+    if (e == cudaSuccess) e = dev_alloc(&h->tile_first, first.size());
+    if (e == cudaSuccess) e = dev_alloc(&h->numel, numel.size());
+    if (e == cudaSuccess && h->mode == LIONCUB_MODE_L1_INTSUM) {
+        e = dev_alloc(&h->partials, static_cast<size_t>(W) * h->ntiles);
+        if (e == cudaSuccess) e = dev_alloc(&h->m1, static_cast<size_t>(W) * h->K);
+        if (e == cudaSuccess) e = dev_alloc(&h->inv, static_cast<size_t>(W) * h->K);
+    }
+    if (e == cudaSuccess && !tiles.empty())
+        e = cudaMemcpy(h->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->tile_first, first.data(), first.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !numel.empty())
+        e = cudaMemcpy(h->numel, numel.data(), numel.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemset(h->wire, 0, (static_cast<size_t>(W) * h->wire_stride + 4) * sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        const int code = (e == cudaErrorMemoryAllocation) ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA;
+        cudaGetLastError();  // clear a non-sticky allocation error
+        free_scratch(h);
+        delete h;
+        return fail(nullptr, code, "device set-up failed: %s", cudaGetErrorString(e));
+    }
+    *out = h;
+    return LIONCUB_OK;
+}
+
+int lioncub_bind_state(lioncub_t h, float* theta, float* const* m)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!theta || !m)
+        return fail(h, LIONCUB_ERR_ARG, "theta and m must be non-NULL");
+    if (!aligned16(theta))
+        return fail(h, LIONCUB_ERR_ALIGN, "theta is not 16-byte aligned");
+    for (int i = 0; i < h->W; ++i) {
+        if (!m[i])
+            return fail(h, LIONCUB_ERR_ARG, "m[%d] is NULL", i);
+        if (!aligned16(m[i]))
+            return fail(h, LIONCUB_ERR_ALIGN, "m[%d] is not 16-byte aligned", i);
+    }
+    h->theta = theta;
+    for (int i = 0; i < h->W; ++i)
+        h->m[i] = m[i];
+    h->bound = true;
+    h->err.clear();
+    return LIONCUB_OK;
+}
+
+int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!h->bound)
+        return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
+    if (!grads)
+        return fail(h, LIONCUB_ERR_ARG, "grads is NULL");
+    for (int i = 0; i < h->W; ++i) {
+        if (!grads[i])
+            return fail(h, LIONCUB_ERR_ARG, "grads[%d] is NULL", i);
+        if (!aligned16(grads[i]))
+            return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const StepArgs a = make_args(h, grads);
+    const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
+    cudaError_t e;
+    int slot;
+    if (l1) {
+        slot = prof_begin(h, LIONCUB_KERNEL_M1, s);
+        e = lc::launch_m1_partial(a, h->grad_dtype, s);
+        prof_end(h, slot, s);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "m1_partial launch");
+        slot = prof_begin(h, LIONCUB_KERNEL_M1_FINAL, s);
+        e = lc::launch_m1_finalize(a, s);
+        prof_end(h, slot, s);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "m1_finalize launch");
+    }
+    slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
+    e = lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s);
+    prof_end(h, slot, s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "compress launch");
+    slot = prof_begin(h, LIONCUB_KERNEL_REDUCE_APPLY, s);
+    e = lc::launch_reduce_apply(a, l1 ? 1 : 0, s);
+    prof_end(h, slot, s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "reduce_apply launch");
+    h->t += 1;
+    return LIONCUB_OK;
+}
+
+int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
+                      lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!h->bound)
+        return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
+    if (!grads_host || !theta_host_out)
+        return fail(h, LIONCUB_ERR_ARG, "grads_host and theta_host_out must be non-NULL");
+    const size_t gbytes = static_cast<size_t>(h->d) * (h->grad_dtype == LIONCUB_GRAD_BF16 ? 2 : 4);
+    const size_t gstride = (gbytes + 255) / 256 * 256;
+    if (!h->staging) {
+        cudaError_t e = cudaMalloc(&h->staging, gstride * h->W + 256);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            h->staging = nullptr;
+            return fail(h, e == cudaErrorMemoryAllocation ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA,
+                        "staging allocation of %zu bytes failed", gstride * h->W);
+        }
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const void* dev[LIONCUB_MAX_WORKERS];
+    for (int i = 0; i < h->W; ++i) {
+        if (!grads_host[i])
+            return fail(h, LIONCUB_ERR_ARG, "grads_host[%d] is NULL", i);
+        char* dst = static_cast<char*>(h->staging) + gstride * i;
+        dev[i] = dst;
+        if (gbytes) {
+            cudaError_t e = cudaMemcpyAsync(dst, grads_host[i], gbytes, cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess)
+                return cuda_fail(h, e, "gradient upload");
+        }
+    }
+    int rc = lioncub_step(h, dev, stream);
+    if (rc != LIONCUB_OK)
+        return rc;
+    if (h->d) {
+        cudaError_t e = cudaMemcpyAsync(theta_host_out, h->theta, static_cast<size_t>(h->d) * sizeof(float),
+                                        cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "theta download");
+    }
+    return LIONCUB_OK;
+}
+
+int lioncub_set_lr(lioncub_t h, float lr)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    h->lr = lr;
+    return LIONCUB_OK;
+}
+
+int lioncub_get_step(lioncub_t h, int64_t* t)
+{
+    if (!h || !t)
+        return LIONCUB_ERR_ARG;
+    *t = h->t;
+    return LIONCUB_OK;
+}
+
+int lioncub_set_step(lioncub_t h, int64_t t)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (t < 0)
+        return fail(h, LIONCUB_ERR_ARG, "step must be >= 0");
+    h->t = t;
+    return LIONCUB_OK;
+}
+
+int64_t lioncub_wire_words(lioncub_t h)
+{
+    return h ? h->wire_words : -1;
+}
+
+int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!dst_dev)
+        return fail(h, LIONCUB_ERR_ARG, "dst_dev is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    switch (what) {
+    case LIONCUB_EXPORT_WIRE:
+        if (h->wire_words)
+            e = cudaMemcpy2DAsync(dst_dev, h->wire_words * sizeof(uint32_t), h->wire,
+                                  h->wire_stride * sizeof(uint32_t), h->wire_words * sizeof(uint32_t), h->W,
+                                  cudaMemcpyDeviceToDevice, s);
+        break;
+    case LIONCUB_EXPORT_M1:
+        if (h->mode != LIONCUB_MODE_L1_INTSUM)
+            return fail(h, LIONCUB_ERR_STATE, "M1 exists in L1 mode only");
+        e = cudaMemcpyAsync(dst_dev, h->m1, static_cast<size_t>(h->W) * h->K * sizeof(float),
+                            cudaMemcpyDeviceToDevice, s);
+        break;
+    case LIONCUB_EXPORT_AGG: {
+        const StepArgs a = make_args(h, nullptr);
+        e = lc::launch_export_agg(a, h->mode == LIONCUB_MODE_L1_INTSUM ? 1 : 0, static_cast<int32_t*>(dst_dev), s);
+        break;
+    }
+    default:
+        return fail(h, LIONCUB_ERR_ARG, "unknown export %d", what);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "debug export");
+    return LIONCUB_OK;
+}
+
+int lioncub_profile(lioncub_t h, int max_steps)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (max_steps < 0)
+        return fail(h, LIONCUB_ERR_ARG, "max_steps must be >= 0");
+    drop_profile(h);
+    if (max_steps == 0)
+        return LIONCUB_OK;
+    const int launches = max_steps * LIONCUB_KERNEL_COUNT;
+    h->prof_events.resize(2 * static_cast<size_t>(launches));
+    h->prof_kernel.assign(launches, -1);
+    for (size_t i = 0; i < h->prof_events.size(); ++i) {
+        cudaError_t e = cudaEventCreate(&h->prof_events[i]);
+        if (e != cudaSuccess) {
+            h->prof_events.resize(i);
+            drop_profile(h);
+            return cuda_fail(h, e, "event creation");
+        }
+    }
+    h->prof_capacity = launches;
+    return LIONCUB_OK;
+}
+
+int lioncub_profile_read(lioncub_t h, int kernel, double* total_ms, int64_t* launches)
+{
+    if (!h || !total_ms || !launches)
+        return LIONCUB_ERR_ARG;
+    double tot = 0.0;
+    int64_t n = 0;
+    for (int slot = 0; slot < h->prof_used; ++slot) {
+        if (h->prof_kernel[slot] != kernel)
+            continue;
+        cudaError_t e = cudaEventSynchronize(h->prof_events[2 * slot + 1]);
+        float ms = 0.0f;
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&ms, h->prof_events[2 * slot], h->prof_events[2 * slot + 1]);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "reading profile events");
+        tot += ms;
+        ++n;
+    }
+    *total_ms = tot;
+    *launches = n;
+    return LIONCUB_OK;
+}
+
+void lioncub_destroy(lioncub_t h)
+{
+    if (!h)
+        return;
+    cudaDeviceSynchronize();
+    drop_profile(h);
+    free_scratch(h);
+    delete h;
+}
+
+}  // extern "C"

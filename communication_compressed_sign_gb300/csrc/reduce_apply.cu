@@ -1,0 +1,153 @@
+// reduce_apply.cu -- W-way aggregation of the workers' wire words, the
+// global sign, and the parameter update.
+//
+// "Lion Cub: Minimizing Communication Overhead in Distributed Lion", "What
+// carries the argument": the workers exchange a quantized sum of their update
+// vectors, after which a global sign is taken.  In sign mode the sum of the
+// +-1 votes is 2*popcount - W (majority vote; "Communication Efficient
+// Distributed Training with Distributed Lion", "Approach", also gives the
+// average agg/W); in L1 mode it is the integer sum of the Eq. (1) codes.
+// theta then takes the textbook Lion step with decoupled weight decay.
+//
+// One thread per 8 consecutive elements.  Sign mode: the thread reads one
+// byte of every worker's words (its 8 bits) and counts set bits per element
+// with byte-lane counters -- each nibble is spread to four byte lanes by one
+// multiply (bit j of the nibble lands on bit 8j), so one 32-bit add counts
+// four elements at once (exact for W <= 255).  L1 mode: the thread reads
+// 8*n bits per worker and sign-extends each field.  Both read theta with
+// 16-byte loads and write it back once.
+#include "device_common.cuh"
+
+namespace lc {
+namespace {
+
+// Per-element aggregates of 8 consecutive elements starting at e0.
+template <int NB>
+__device__ __forceinline__ void aggregate8(const StepArgs& a, int64_t e0, int* agg)
+{
+    if constexpr (NB == 1) {
+        const uint8_t* wb = reinterpret_cast<const uint8_t*>(a.wire) + (e0 >> 3);
+        const int64_t stride = a.wire_stride * 4;
+        uint32_t lo = 0, hi = 0;
+        for (int i = 0; i < a.W; ++i) {
+            const uint32_t b = wb[static_cast<int64_t>(i) * stride];
+            lo += ((b & 0xfu) * 0x204081u) & 0x01010101u;
+            hi += ((b >> 4) * 0x204081u) & 0x01010101u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            agg[j] = 2 * static_cast<int>((lo >> (8 * j)) & 0xffu) - a.W;
+            agg[j + 4] = 2 * static_cast<int>((hi >> (8 * j)) & 0xffu) - a.W;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            agg[j] = 0;
+        for (int i = 0; i < a.W; ++i) {
+            const uint32_t* wi = a.wire + static_cast<int64_t>(i) * a.wire_stride;
+            if constexpr (NB == 2) {
+                const uint32_t h = reinterpret_cast<const uint16_t*>(wi)[e0 >> 3];
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    agg[j] += static_cast<int32_t>(h << (30 - 2 * j)) >> 30;
+            } else if constexpr (NB == 4) {
+                const uint32_t w = wi[e0 >> 3];
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    agg[j] += static_cast<int32_t>(w << (28 - 4 * j)) >> 28;
+            } else {
+                const uint2 w = *reinterpret_cast<const uint2*>(wi + (e0 >> 2));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    agg[j] += static_cast<int32_t>(w.x << (24 - 8 * j)) >> 24;
+                    agg[j + 4] += static_cast<int32_t>(w.y << (24 - 8 * j)) >> 24;
+                }
+            }
+        }
+    }
+}
+
+// Update direction u from the aggregate: the global sign (a tie gives tie_u),
+// or agg / W for the D-Lion average.
+__device__ __forceinline__ float direction(const StepArgs& a, int agg)
+{
+    if (a.average)
+        return __fdiv_rn(static_cast<float>(agg), static_cast<float>(a.W));
+    return agg > 0 ? 1.0f : (agg < 0 ? -1.0f : a.tie_u);
+}
+
+// theta' = theta - lr * (u + wd * theta)
+__device__ __forceinline__ float lion_apply(float theta, float u, float lr, float wd)
+{
+    return __fsub_rn(theta, __fmul_rn(lr, __fadd_rn(u, __fmul_rn(wd, theta))));
+}
+
+template <int NB>
+__global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
+{
+    const int64_t e0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kVec;
+    if (e0 >= a.d)
+        return;
+    const int valid = (a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0);
+    int agg[kVec];
+    aggregate8<NB>(a, e0, agg);
+    float th[kVec];
+    load_f32(a.theta, e0, valid, th);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j)
+        th[j] = lion_apply(th[j], direction(a, agg[j]), a.lr, a.wd);
+    store_f32(a.theta, e0, valid, th);
+}
+
+template <int NB>
+__global__ void __launch_bounds__(256) k_export_agg(const StepArgs a, int32_t* out)
+{
+    const int64_t e0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kVec;
+    if (e0 >= a.d)
+        return;
+    const int valid = (a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0);
+    int agg[kVec];
+    aggregate8<NB>(a, e0, agg);
+    for (int j = 0; j < valid; ++j)
+        out[e0 + j] = agg[j];
+}
+
+unsigned groups_grid(int64_t d)
+{
+    const int64_t groups = (d + kVec - 1) / kVec;
+    return static_cast<unsigned>((groups + 255) / 256);
+}
+
+}  // namespace
+
+cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s)
+{
+    if (a.d == 0)
+        return cudaSuccess;
+    const unsigned grid = groups_grid(a.d);
+    switch (l1_mode ? a.nbits : 1) {
+    case 1: k_reduce_apply<1><<<grid, 256, 0, s>>>(a); break;
+    case 2: k_reduce_apply<2><<<grid, 256, 0, s>>>(a); break;
+    case 4: k_reduce_apply<4><<<grid, 256, 0, s>>>(a); break;
+    case 8: k_reduce_apply<8><<<grid, 256, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s)
+{
+    if (a.d == 0)
+        return cudaSuccess;
+    const unsigned grid = groups_grid(a.d);
+    switch (l1_mode ? a.nbits : 1) {
+    case 1: k_export_agg<1><<<grid, 256, 0, s>>>(a, agg); break;
+    case 2: k_export_agg<2><<<grid, 256, 0, s>>>(a, agg); break;
+    case 4: k_export_agg<4><<<grid, 256, 0, s>>>(a, agg); break;
+    case 8: k_export_agg<8><<<grid, 256, 0, s>>>(a, agg); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lc

@@ -1,0 +1,180 @@
+"""ctypes binding of liblioncub.so (the C ABI in include/lioncub.h).
+
+Argument marshalling only: every step of the method runs in the library's
+CUDA kernels.  Functions keep the C names; pointers are passed as Python
+ints (for example ``tensor.data_ptr()``) and streams as the raw
+``cudaStream_t`` value (``torch.cuda.Stream.cuda_stream``).  A non-zero
+return code raises :class:`LionCubError` with the library's message.
+
+If the library has not been built the first call raises; there is no other
+implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblioncub.so")
+
+# enums of include/lioncub.h
+TENSOR_SYNC_M = 1
+MODE_SIGN_MAJORITY = 0
+MODE_L1_INTSUM = 1
+FLAG_TIE_ALTERNATE = 0x100
+FLAG_AVERAGE = 0x200
+GRAD_BF16 = 0
+GRAD_F32 = 1
+OK, ERR_ARG, ERR_ALIGN, ERR_STATE, ERR_OOM, ERR_CUDA = 0, -1, -2, -3, -4, -5
+MAX_WORKERS = 128
+EXPORT_WIRE, EXPORT_M1, EXPORT_AGG = 0, 1, 2
+KERNEL_COMPRESS, KERNEL_M1, KERNEL_M1_FINAL, KERNEL_REDUCE_APPLY, KERNEL_COUNT = 0, 1, 2, 3, 4
+KERNEL_NAMES = {KERNEL_COMPRESS: "compress", KERNEL_M1: "m1_partial",
+                KERNEL_M1_FINAL: "m1_finalize", KERNEL_REDUCE_APPLY: "reduce_apply"}
+
+# Every symbol the header declares, for load checks.
+EXPORTED = (
+    "lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
+    "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step", "lioncub_wire_words",
+    "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read",
+    "lioncub_last_error", "lioncub_strerror", "lioncub_destroy",
+)
+
+
+class LionCubError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{message} [{code}]")
+        self.code = code
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_int64), ("numel", ctypes.c_int64), ("flags", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblioncub.so (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m communication_compressed_sign_gb300.build`")
+        L = ctypes.CDLL(path)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        L.lioncub_create.argtypes = [ctypes.POINTER(vp), i64, i32, vp, i32, f32, f32, f32, f32, i32,
+                                     i32, i32, i32]
+        L.lioncub_bind_state.argtypes = [vp, vp, vp]
+        L.lioncub_step.argtypes = [vp, vp, vp]
+        L.lioncub_step_host.argtypes = [vp, vp, vp, vp]
+        L.lioncub_set_lr.argtypes = [vp, f32]
+        L.lioncub_get_step.argtypes = [vp, ctypes.POINTER(i64)]
+        L.lioncub_set_step.argtypes = [vp, i64]
+        L.lioncub_wire_words.argtypes = [vp]
+        L.lioncub_wire_words.restype = i64
+        L.lioncub_debug_export.argtypes = [vp, i32, vp, vp]
+        L.lioncub_profile.argtypes = [vp, i32]
+        L.lioncub_profile_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
+        L.lioncub_last_error.argtypes = [vp]
+        L.lioncub_last_error.restype = ctypes.c_char_p
+        L.lioncub_strerror.argtypes = [i32]
+        L.lioncub_strerror.restype = ctypes.c_char_p
+        L.lioncub_destroy.argtypes = [vp]
+        L.lioncub_destroy.restype = None
+        for name in ("lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
+                     "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step",
+                     "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read"):
+            getattr(L, name).restype = i32
+        _lib = L
+        return L
+
+
+def _check(rc: int, h) -> None:
+    if rc != OK:
+        L = load()
+        msg = L.lioncub_last_error(h).decode() or L.lioncub_strerror(rc).decode()
+        raise LionCubError(rc, msg)
+
+
+def _ptrs(values) -> ctypes.Array:
+    return (ctypes.c_void_p * len(values))(*[int(v) for v in values])
+
+
+def lioncub_create(d: int, W: int, layout, beta1: float, beta2: float, lr: float, wd: float,
+                   mode: int, nbits: int, grad_dtype: int, sync_interval: int) -> int:
+    """layout: sequence of (offset, numel, flags), or None/empty for one tensor."""
+    L = load()
+    h = ctypes.c_void_p()
+    if layout:
+        arr = (Tensor * len(layout))(*[Tensor(int(o), int(n), int(f)) for (o, n, f) in layout])
+        lp, K = ctypes.cast(arr, ctypes.c_void_p), len(layout)
+    else:
+        lp, K = None, 0
+    rc = L.lioncub_create(ctypes.byref(h), d, W, lp, K, beta1, beta2, lr, wd, mode, nbits, grad_dtype,
+                          sync_interval)
+    _check(rc, None)
+    return h.value
+
+
+def lioncub_bind_state(h: int, theta_ptr: int, m_ptrs) -> None:
+    _check(load().lioncub_bind_state(h, theta_ptr, ctypes.cast(_ptrs(m_ptrs), ctypes.c_void_p)), h)
+
+
+def lioncub_step(h: int, grad_ptrs, stream: int = 0) -> None:
+    _check(load().lioncub_step(h, ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), stream or None), h)
+
+
+def lioncub_step_host(h: int, grad_host_ptrs, theta_host_out_ptr: int, stream: int = 0) -> None:
+    _check(load().lioncub_step_host(h, ctypes.cast(_ptrs(grad_host_ptrs), ctypes.c_void_p),
+                                    theta_host_out_ptr, stream or None), h)
+
+
+def lioncub_set_lr(h: int, lr: float) -> None:
+    _check(load().lioncub_set_lr(h, lr), h)
+
+
+def lioncub_get_step(h: int) -> int:
+    t = ctypes.c_int64()
+    _check(load().lioncub_get_step(h, ctypes.byref(t)), h)
+    return t.value
+
+
+def lioncub_set_step(h: int, t: int) -> None:
+    _check(load().lioncub_set_step(h, t), h)
+
+
+def lioncub_wire_words(h: int) -> int:
+    return load().lioncub_wire_words(h)
+
+
+def lioncub_debug_export(h: int, what: int, dst_ptr: int, stream: int = 0) -> None:
+    _check(load().lioncub_debug_export(h, what, dst_ptr, stream or None), h)
+
+
+def lioncub_profile(h: int, max_steps: int) -> None:
+    _check(load().lioncub_profile(h, max_steps), h)
+
+
+def lioncub_profile_read(h: int, kernel: int):
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(load().lioncub_profile_read(h, kernel, ctypes.byref(ms), ctypes.byref(n)), h)
+    return ms.value, n.value
+
+
+def lioncub_last_error(h) -> str:
+    return load().lioncub_last_error(h).decode()
+
+
+def lioncub_strerror(code: int) -> str:
+    return load().lioncub_strerror(code).decode()
+
+
+def lioncub_destroy(h: int) -> None:
+    if h:
+        load().lioncub_destroy(h)

@@ -1,0 +1,210 @@
+/*
+ * lioncub.h -- C ABI of the GB300 library for the compressed Lion update step
+ * of Lion Cub / Distributed Lion, with W data-parallel workers simulated as W
+ * gradient and momentum buffers resident in one GPU's memory.
+ *
+ * Sources (page title, then the part of the page):
+ *   [LC] "Lion Cub: Minimizing Communication Overhead in Distributed Lion"
+ *        (machine review page): "What carries the argument" -- the update
+ *        vector c_{i,t} = beta1 m_{i,t-1} + (1-beta1) grad f_i(theta_{t-1}),
+ *        signs packed as 0/1 with exact zeros sent as +1/-1 on alternating
+ *        iterations, the L1 quantizer of Eq. (1)
+ *        Q1(x) = clamp(round((2^(n-1)-1) x / M1(x)), 2^(n-1)-1) with M1 the
+ *        mean absolute value, a quantized sum followed by a global sign, and
+ *        momentum synchronized only on the input-embedding and output
+ *        layers; the Fig. 1 and Fig. 8 captions (1-bit and p-bit allreduce);
+ *        the assumptions list (sync every 10 iterations).
+ *   [DL] "Communication Efficient Distributed Training with Distributed
+ *        Lion" (summary page): "Approach" -- each worker keeps its own Lion
+ *        momentum and sends the sign of its local update; the aggregate is
+ *        the majority vote (MaVo) or the average (Avg).
+ *   The theta and momentum rules are textbook Lion (Chen et al. 2023), which
+ *   both pages cite.
+ *
+ * One step, with t the 0-based step index:
+ *   c_i   = RN(RN(beta1*m_i) + RN(omega1*g_i)),  omega1 = RN(1 - beta1)
+ *   sign mode:  bit_i = 1 if c_i > 0, 0 if c_i < 0, (t even ? 1 : 0) if c_i == 0
+ *               agg = sum_i (2*bit_i - 1)                      in [-W, W]
+ *   L1 mode:    M1_{i,k} = mean over tensor k of |c_i| (fp64 sum, one
+ *               rounding to fp32); inv = RN(qmax / M1);
+ *               q_i = clamp(rint(RN(c_i*inv)), -qmax, qmax), qmax = 2^(n-1)-1
+ *               (q = 0 where M1 == 0); agg = sum_i q_i
+ *   u     = sign(agg) in {-1, 0, +1}  (ties give 0); with
+ *           LIONCUB_FLAG_TIE_ALTERNATE a tie gives t even ? +1 : -1; with
+ *           LIONCUB_FLAG_AVERAGE (sign mode only) u = RN(agg / W)
+ *   theta = RN(theta - RN(lr * RN(u + RN(wd*theta))))
+ *   m_i   = RN(RN(beta2*m_i) + RN(omega2*g_i)),  omega2 = RN(1 - beta2)
+ *   sync: on tensors flagged LIONCUB_TENSOR_SYNC_M, when sync_interval > 0
+ *         and (t+1) % sync_interval == 0: s = m_0; s = RN(s + m_j) for
+ *         j = 1..W-1; every m_i = RN(s / W)
+ *   t     = t + 1
+ * RN is one IEEE fp32 rounding to nearest-even; no multiply-add is fused.
+ *
+ * Wire format (what a real worker would send): sign mode packs element e of
+ * worker i into bit e%32 of word e/32 (LSB first, 1 = +1); L1 mode packs
+ * two's-complement n-bit codes, 32/n per word, element e in field e%(32/n)
+ * of word e*n/32.  Bits past d are 0.
+ *
+ * Return codes: LIONCUB_OK (0) or a negative LIONCUB_ERR_*.  After an error,
+ * lioncub_last_error(h) describes it.  Kernel faults are asynchronous: they
+ * surface as LIONCUB_ERR_CUDA at a later call or at the caller's stream
+ * synchronization.  No call synchronizes the device except the ones marked
+ * "synchronizes".
+ */
+#ifndef LIONCUB_H
+#define LIONCUB_H
+
+#include <stdint.h>
+
+/* Exported entry points keep default visibility even when the library is
+ * built with hidden visibility. */
+#if defined(__GNUC__)
+#define LIONCUB_API __attribute__((visibility("default")))
+#else
+#define LIONCUB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lioncub_s* lioncub_t;
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* lioncub_stream_t;
+
+/* One tensor of the flat parameter vector: elements [offset, offset+numel).
+ * The tensors of a layout tile [0, d) in order, and every offset is a
+ * multiple of 32 elements (so a packed word never spans two tensors). */
+typedef struct {
+    int64_t offset;
+    int64_t numel;
+    uint32_t flags; /* LIONCUB_TENSOR_SYNC_M or 0 */
+} lioncub_tensor;
+
+enum {
+    LIONCUB_TENSOR_SYNC_M = 1 /* average this tensor's momentum across workers */
+};
+
+enum {
+    LIONCUB_MODE_SIGN_MAJORITY = 0, /* 1-bit signs, majority vote          */
+    LIONCUB_MODE_L1_INTSUM = 1,     /* n-bit Eq. (1) codes, integer sum    */
+    LIONCUB_FLAG_TIE_ALTERNATE = 0x100, /* OR into mode: tie -> step's zero sign */
+    LIONCUB_FLAG_AVERAGE = 0x200        /* OR into mode: D-Lion Avg, u = agg/W  */
+};
+
+enum { LIONCUB_GRAD_BF16 = 0, LIONCUB_GRAD_F32 = 1 };
+
+enum {
+    LIONCUB_OK = 0,
+    LIONCUB_ERR_ARG = -1,   /* invalid argument                                 */
+    LIONCUB_ERR_ALIGN = -2, /* offset not a multiple of 32 / pointer not 16-byte */
+    LIONCUB_ERR_STATE = -3, /* state not bound, or call out of order            */
+    LIONCUB_ERR_OOM = -4,   /* device or host allocation failed                 */
+    LIONCUB_ERR_CUDA = -5   /* a CUDA call or launch failed                     */
+};
+
+enum { LIONCUB_MAX_WORKERS = 128 };
+
+/* What lioncub_debug_export copies. */
+enum {
+    LIONCUB_EXPORT_WIRE = 0, /* W x lioncub_wire_words() uint32: last step's packed words/codes */
+    LIONCUB_EXPORT_M1 = 1,   /* W x K float: last step's M1 (L1 mode)               */
+    LIONCUB_EXPORT_AGG = 2   /* d int32: the aggregate of the last step's wire words */
+};
+
+/* Kernels whose launches lioncub_profile_read reports. */
+enum {
+    LIONCUB_KERNEL_COMPRESS = 0,     /* c, sign bits or Q1 codes, momentum, sync */
+    LIONCUB_KERNEL_M1 = 1,           /* per-tile fp64 sums of |c| (L1 mode)      */
+    LIONCUB_KERNEL_M1_FINAL = 2,     /* per-tensor M1 and 1/M1 scale (L1 mode)   */
+    LIONCUB_KERNEL_REDUCE_APPLY = 3, /* W-way vote / integer sum, sign, theta    */
+    LIONCUB_KERNEL_COUNT = 4
+};
+
+/*
+ * Create a handle for d parameters, W workers (1..LIONCUB_MAX_WORKERS) and a
+ * layout of K tensors (layout may be NULL with K == 0: one tensor [0, d)).
+ * mode: LIONCUB_MODE_* optionally OR'ed with LIONCUB_FLAG_*.  nbits: 2, 4 or
+ * 8 in L1 mode (ignored in sign mode).  grad_dtype: LIONCUB_GRAD_*.
+ * sync_interval: 0 = never sync, else sync flagged tensors every
+ * sync_interval steps.  The library allocates its own device scratch (wire
+ * words or codes, M1 partials, tile table) here and frees it in
+ * lioncub_destroy; the caller's layout array is copied.  Errors: ERR_ARG,
+ * ERR_ALIGN, ERR_OOM, ERR_CUDA (*out is set to NULL).  Uses the current
+ * CUDA device, which must stay current for every later call on the handle.
+ */
+LIONCUB_API int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layout, int K,
+                   float beta1, float beta2, float lr, float wd, int mode, int nbits,
+                   int grad_dtype, int sync_interval);
+
+/*
+ * Bind the optimizer state: theta (d fp32, device) and m[0..W-1] (W device
+ * pointers to d fp32 each; the host array is read during the call only).
+ * The caller owns the memory and keeps it alive while the handle uses it.
+ * Every pointer must be 16-byte aligned (ERR_ALIGN), non-NULL (ERR_ARG).
+ */
+LIONCUB_API int lioncub_bind_state(lioncub_t h, float* theta, float* const* m);
+
+/*
+ * Enqueue one step on `stream`: grads[0..W-1] are W device pointers to d
+ * gradients of the handle's dtype, 16-byte aligned; the host array is read
+ * during the call only, the device buffers must stay unchanged until the
+ * step has run.  theta and m are updated in place; the step counter advances
+ * only if every launch was enqueued.  Errors: ERR_STATE (unbound), ERR_ARG,
+ * ERR_ALIGN, ERR_CUDA.  Does not synchronize.
+ */
+LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream);
+
+/*
+ * The same step fed from host memory: copies grads_host[0..W-1] (W host
+ * buffers of d gradients; page-locked memory gives full copy speed) into
+ * library-owned device staging (allocated on the first call, kept until
+ * destroy), runs the step, and copies the updated theta into theta_host_out
+ * (d floats, host).  All copies are enqueued on `stream`; the host buffers
+ * must stay valid until the stream has finished.  Errors as lioncub_step,
+ * plus ERR_OOM for the staging.
+ */
+LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
+                      lioncub_stream_t stream);
+
+LIONCUB_API int lioncub_set_lr(lioncub_t h, float lr);
+/* Step counter t (the parity of t decides the sign of an exact zero). */
+LIONCUB_API int lioncub_get_step(lioncub_t h, int64_t* t);
+LIONCUB_API int lioncub_set_step(lioncub_t h, int64_t t);
+
+/* Words per worker of the wire buffer: ceil(d/32) in sign mode, ceil(d*n/32)
+ * in L1 mode; -1 for a NULL handle. */
+LIONCUB_API int64_t lioncub_wire_words(lioncub_t h);
+
+/*
+ * Copy diagnostic data of the last step into dst_dev (device memory the
+ * caller owns; sizes in the LIONCUB_EXPORT_* comments) on `stream`.  For
+ * LIONCUB_EXPORT_AGG a kernel recomputes the aggregate from the wire words.
+ * For tests; never part of a timed step.
+ */
+LIONCUB_API int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t stream);
+
+/*
+ * Per-kernel timing with CUDA events on the step's stream.  lioncub_profile
+ * (h, n) records an event pair around every launch of the next n steps
+ * (n == 0 turns recording off and drops the records).  lioncub_profile_read
+ * (synchronizes on the recorded events) gives, for one LIONCUB_KERNEL_*, the
+ * summed milliseconds and the number of launches recorded.
+ */
+LIONCUB_API int lioncub_profile(lioncub_t h, int max_steps);
+LIONCUB_API int lioncub_profile_read(lioncub_t h, int kernel, double* total_ms, int64_t* launches);
+
+/* Message for the last error on h (never NULL; "" when none).  With h ==
+ * NULL: the message of the last failed lioncub_create on this thread. */
+LIONCUB_API const char* lioncub_last_error(lioncub_t h);
+/* Static name of a LIONCUB_* return code. */
+LIONCUB_API const char* lioncub_strerror(int code);
+
+/* Free the handle's scratch and events.  Synchronizes the device first, so
+ * no enqueued step still uses the scratch.  NULL is a no-op. */
+LIONCUB_API void lioncub_destroy(lioncub_t h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIONCUB_H */

@@ -1,0 +1,242 @@
+"""GPU-vs-oracle parity harness (used by the gpu-marked tests and smoke()).
+
+The CUDA library runs the whole workload on the GPU through its C ABI; the
+CPU oracle runs the same steps on a set of *pieces* of the flat parameter
+vector, fed with a host copy of exactly the gradient bits the GPU used.  In
+sign mode every element is independent, so any 32-aligned piece is a valid
+sub-problem; in L1 mode M1 spans a whole tensor, so pieces are whole
+tensors.  After every step the harness compares, piece by piece, the wire
+words, the aggregates, M1 (L1 mode), theta and the momenta.
+
+Tolerances (sign mode: everything bit-exact):
+  L1 mode -- M1 within 1e-6 relative; codes differ by at most one quantum on
+  at most 1e-5 of the elements (near-ties that follow from the last bits of
+  M1, whose fp64 summation order differs); theta within 1e-6 relative except
+  at elements whose aggregate differed at some step; momenta bit-exact (they
+  do not depend on the quantization).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle
+import synth
+from communication_compressed_sign_gb300 import lioncub as lc
+
+M1_RTOL = 1e-6
+CODE_FRAC = 1e-5
+THETA_RTOL = 1e-6
+
+
+@dataclass
+class Piece:
+    src: int        # offset in the full flat vector (multiple of 32)
+    n: int
+    flags: int
+    tensor: int     # index of the tensor in the full layout (for M1), -1 if partial
+
+
+def tensor_pieces(layout, names):
+    out = []
+    for k, (name, off, n, fl) in enumerate(layout):
+        if name in names:
+            out.append(Piece(off, n, fl, k))
+    return out
+
+
+def chunk_pieces(layout, name, count, length, seed=0):
+    """`count` random 32-aligned chunks of `length` elements inside tensor `name`."""
+    k = [i for i, t in enumerate(layout) if t[0] == name][0]
+    _, off, n, fl = layout[k]
+    rng = np.random.default_rng(seed)
+    starts = sorted(set(int(s) * 32 for s in rng.integers(0, (n - length) // 32, size=count)))
+    res, last = [], -1
+    for s in starts:
+        if s < last:
+            continue
+        res.append(Piece(off + s, length, fl, -1))
+        last = s + length
+    return res
+
+
+def _words_range(p: Piece, bits: int):
+    w0 = p.src * bits // 32
+    return w0, (p.n * bits + 31) // 32
+
+
+@dataclass
+class ParityReport:
+    steps: int = 0
+    elements: int = 0
+    wire_mismatch_words: int = 0
+    agg_mismatch: int = 0
+    code_offby1: int = 0
+    code_worse: int = 0
+    m1_max_rel: float = 0.0
+    m1_inexact: int = 0
+    theta_max_rel: float = 0.0
+    theta_mismatch: int = 0
+    theta_mismatch_outside_agg: int = 0
+    m_mismatch: int = 0
+
+
+def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, strict: bool = True,
+               use_host_step: bool = False, grad_hook=None):
+    """Run `steps` steps of workload `wl` on the GPU and on the oracle (over
+    `pieces`); return a ParityReport.  With strict=True, assert the bounds.
+    grad_hook(t, i, tensor), if given, edits worker i's step-t gradients on
+    the GPU after they are generated (both sides see the edited bits)."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    W, d = wl.W, wl.d
+    l1 = wl.mode == 1
+    bits = wl.nbits if l1 else 1
+    gdt = synth.grad_dtype(wl)
+
+    theta = torch.empty(d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+    grads = [torch.empty(d, dtype=gdt, device=dev) for _ in range(W)]
+
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
+                          wl.mode | mode_flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
+                          wl.sync_interval)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        nwords = lc.lioncub_wire_words(h)
+        wire = torch.empty((W, max(nwords, 1)), dtype=torch.int32, device=dev)
+        agg = torch.empty(max(d, 1), dtype=torch.int32, device=dev)
+        K = len(wl.layout)
+        m1 = torch.empty((W, K), dtype=torch.float32, device=dev) if l1 else None
+
+        # oracle sub-problem: the pieces laid end to end (inner pieces have
+        # 32-multiple lengths, so every destination offset stays 32-aligned)
+        for p in pieces[:-1]:
+            assert p.n % 32 == 0, "inner pieces must have 32-multiple lengths"
+        dsub = sum(p.n for p in pieces)
+        sub_layout, dst = [], 0
+        for p in pieces:
+            sub_layout.append((dst, p.n, p.flags))
+            dst += p.n
+        if l1:
+            assert all(p.tensor >= 0 for p in pieces), "L1 mode needs whole-tensor pieces (M1 is per tensor)"
+        idx = torch.cat([torch.arange(p.src, p.src + p.n, device=dev) for p in pieces])
+        wranges = [_words_range(p, bits) for p in pieces]
+        widx = torch.cat([torch.arange(w0, w0 + nw, device=dev) for (w0, nw) in wranges])
+        theta_o = theta[idx].cpu().numpy().copy()
+        m_o = [np.zeros(dsub, np.float32) for _ in range(W)]
+        rep = ParityReport(elements=dsub)
+        agg_diverged = np.zeros(dsub, bool)
+        stream = torch.cuda.current_stream()
+
+        pinned = None
+        theta_host = None
+        if use_host_step:
+            pinned = [torch.empty(d, dtype=gdt).pin_memory() for _ in range(W)]
+            theta_host = torch.empty(d, dtype=torch.float32).pin_memory()
+
+        for t in range(steps):
+            for i in range(W):
+                synth.fill_grad_(grads[i], wl, t, i)
+                if grad_hook is not None:
+                    grad_hook(t, i, grads[i])
+            g_o = []
+            for i in range(W):
+                gi = grads[i][idx].cpu()
+                g_o.append(gi.view(torch.int16).numpy().view(np.uint16).copy() if wl.grad == "bf16"
+                           else gi.numpy().copy())
+            if use_host_step:
+                for i in range(W):
+                    pinned[i].copy_(grads[i])
+                torch.cuda.synchronize()
+                lc.lioncub_step_host(h, [x.data_ptr() for x in pinned], theta_host.data_ptr(),
+                                     stream.cuda_stream)
+            else:
+                lc.lioncub_step(h, [g.data_ptr() for g in grads], stream.cuda_stream)
+            lc.lioncub_debug_export(h, lc.EXPORT_WIRE, wire.data_ptr(), stream.cuda_stream)
+            lc.lioncub_debug_export(h, lc.EXPORT_AGG, agg.data_ptr(), stream.cuda_stream)
+            if l1:
+                lc.lioncub_debug_export(h, lc.EXPORT_M1, m1.data_ptr(), stream.cuda_stream)
+            torch.cuda.synchronize()
+            if use_host_step:
+                assert torch.equal(theta_host, theta.cpu()), "host-step theta copy differs from device theta"
+
+            out = oracle.step(d=dsub, W=W, layout=sub_layout, beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr,
+                              wd=wl.wd, mode=wl.mode, nbits=wl.nbits, flags=mode_flags,
+                              sync_interval=wl.sync_interval, t=t, grads=g_o, theta=theta_o, m=m_o)
+            rep.steps += 1
+            wire_h = wire[:, widx].cpu().numpy().view(np.uint32)
+            agg_h = agg[idx].cpu().numpy()
+            agg_diff = agg_h != out.agg
+            rep.agg_mismatch += int(agg_diff.sum())
+            agg_diverged |= agg_diff
+
+            # wire words / codes
+            dst, gsel = 0, 0
+            for p, (_, nw) in zip(pieces, wranges):
+                ow0 = dst * bits // 32
+                for i in range(W):
+                    gw = wire_h[i, gsel:gsel + nw]
+                    ow = out.wire[i][ow0:ow0 + nw]
+                    neq = gw != ow
+                    if neq.any():
+                        rep.wire_mismatch_words += int(neq.sum())
+                        if l1:
+                            gc = _decode(gw, bits, p.n)
+                            oc = _decode(ow, bits, p.n)
+                            dd = np.abs(gc - oc)
+                            rep.code_offby1 += int((dd == 1).sum())
+                            rep.code_worse += int((dd > 1).sum())
+                if l1 and p.tensor >= 0:
+                    k_sub = pieces.index(p)
+                    g_m1 = m1[:, p.tensor].cpu().numpy()
+                    o_m1 = out.m1[:, k_sub]
+                    rel = np.abs(g_m1.astype(np.float64) - o_m1) / np.maximum(np.abs(o_m1), 1e-30)
+                    rep.m1_max_rel = max(rep.m1_max_rel, float(rel.max()))
+                    rep.m1_inexact += int((g_m1 != o_m1).sum())
+                dst += p.n
+                gsel += nw
+
+            th_g = theta[idx].cpu().numpy()
+            neq = th_g.view(np.uint32) != theta_o.view(np.uint32)
+            rep.theta_mismatch = int(neq.sum())
+            rep.theta_mismatch_outside_agg = int((neq & ~agg_diverged).sum())
+            rel = np.abs(th_g.astype(np.float64) - theta_o) / np.maximum(np.abs(theta_o), 1e-30)
+            rel_ok = rel[~agg_diverged]
+            rep.theta_max_rel = float(rel_ok.max()) if rel_ok.size else 0.0
+            mm = 0
+            for i in range(W):
+                mm += int((m[i][idx].cpu().numpy().view(np.uint32) != m_o[i].view(np.uint32)).sum())
+            rep.m_mismatch = mm
+
+            if strict:
+                _assert_bounds(rep, l1, W, t)
+        return rep
+    finally:
+        lc.lioncub_destroy(h)
+
+
+def _decode(words, bits, n):
+    per = 32 // bits
+    e = np.arange(n)
+    f = (words[e // per].astype(np.int64) >> (bits * (e % per))) & ((1 << bits) - 1)
+    return np.where(f >= (1 << (bits - 1)), f - (1 << bits), f)
+
+
+def _assert_bounds(rep: ParityReport, l1: bool, W: int, t: int):
+    if not l1:
+        assert rep.wire_mismatch_words == 0, f"step {t}: packed sign words differ: {rep}"
+        assert rep.agg_mismatch == 0, f"step {t}: vote counts differ: {rep}"
+        assert rep.theta_mismatch == 0, f"step {t}: theta differs: {rep}"
+        assert rep.m_mismatch == 0, f"step {t}: momentum differs: {rep}"
+    else:
+        assert rep.m1_max_rel <= M1_RTOL, f"step {t}: M1 beyond {M1_RTOL} relative: {rep}"
+        assert rep.code_worse == 0, f"step {t}: a code differs by more than one quantum: {rep}"
+        limit = CODE_FRAC * rep.elements * W * rep.steps
+        assert rep.code_offby1 <= max(limit, 0), f"step {t}: too many off-by-one codes: {rep}"
+        assert rep.theta_max_rel <= THETA_RTOL, f"step {t}: theta beyond {THETA_RTOL}: {rep}"
+        assert rep.theta_mismatch_outside_agg == 0, f"step {t}: theta differs where the aggregate agreed: {rep}"
+        assert rep.m_mismatch == 0, f"step {t}: momentum differs: {rep}"

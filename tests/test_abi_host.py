@@ -1,0 +1,119 @@
+"""Host-only checks of the C ABI library and the workload definitions.
+
+No GPU is touched: the library is loaded, every symbol that include/lioncub.h
+declares must be exported, and argument validation (which runs before any
+CUDA call) must return the documented codes.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lc():
+    from communication_compressed_sign_gb300 import build
+    build.build()
+    from communication_compressed_sign_gb300 import lioncub
+    lioncub.load()
+    return lioncub
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "lioncub.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"LIONCUB_API[^;(]*?\b(lioncub_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lc):
+    declared = _declared()
+    assert len(declared) == 14
+    lib = ctypes.CDLL(lc.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(lc.EXPORTED) == declared
+
+
+def test_create_validation_codes(lc):
+    L = lc.load()
+    h = ctypes.c_void_p()
+
+    def create(d, W, layout, mode=0, nbits=1, grad=0, interval=0):
+        if layout:
+            arr = (lc.Tensor * len(layout))(*[lc.Tensor(*t) for t in layout])
+            return L.lioncub_create(ctypes.byref(h), d, W, ctypes.cast(arr, ctypes.c_void_p), len(layout),
+                                    0.9, 0.99, 1e-4, 0.1, mode, nbits, grad, interval)
+        return L.lioncub_create(ctypes.byref(h), d, W, None, 0, 0.9, 0.99, 1e-4, 0.1, mode, nbits, grad,
+                                interval)
+
+    assert create(100, 0, None) == lc.ERR_ARG
+    assert create(100, lc.MAX_WORKERS + 1, None) == lc.ERR_ARG
+    assert create(-1, 2, None) == lc.ERR_ARG
+    assert create(100, 2, None, mode=1, nbits=3) == lc.ERR_ARG
+    assert "nbits" in lc.lioncub_last_error(None)
+    assert create(100, 2, None, mode=7) == lc.ERR_ARG
+    assert create(100, 2, None, grad=5) == lc.ERR_ARG
+    assert create(100, 2, None, interval=-1) == lc.ERR_ARG
+    assert create(100, 2, None, mode=1 | lc.FLAG_AVERAGE, nbits=4) == lc.ERR_ARG
+    assert create(100, 2, None, mode=lc.FLAG_AVERAGE | lc.FLAG_TIE_ALTERNATE) == lc.ERR_ARG
+    assert create(100, 2, None, mode=0x400) == lc.ERR_ARG
+    assert create(64, 2, [(0, 40, 0), (40, 24, 0)]) == lc.ERR_ALIGN
+    assert "multiple of 32" in lc.lioncub_last_error(None)
+    assert create(64, 2, [(0, 32, 0), (48, 16, 0)]) == lc.ERR_ALIGN
+    assert create(64, 2, [(0, 32, 0), (32, 16, 0)]) == lc.ERR_ARG      # does not reach d
+    assert create(64, 2, [(0, 32, 0), (0, 32, 0)]) == lc.ERR_ARG       # overlaps
+    assert create(64, 2, [(0, 64, 4)]) == lc.ERR_ARG                   # unknown tensor flag
+    assert h.value is None
+
+
+def test_null_handle_paths(lc):
+    L = lc.load()
+    assert L.lioncub_step(None, None, None) == lc.ERR_ARG
+    assert L.lioncub_bind_state(None, None, None) == lc.ERR_ARG
+    assert L.lioncub_wire_words(None) == -1
+    assert L.lioncub_set_lr(None, 1.0) == lc.ERR_ARG
+    L.lioncub_destroy(None)
+    assert lc.lioncub_strerror(lc.ERR_ALIGN) == "LIONCUB_ERR_ALIGN"
+    assert lc.lioncub_strerror(-99) == "LIONCUB_ERR_UNKNOWN"
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from communication_compressed_sign_gb300 import lioncub
+    saved = lioncub._lib
+    lioncub._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            lioncub.load(str(tmp_path / "liblioncub.so"))
+    finally:
+        lioncub._lib = saved
+
+
+@pytest.mark.parametrize("key,d,K", [(1, 1_048_576, 1), (2, 124_439_808, 148), (3, 354_823_168, 292),
+                                     (4, 354_823_168, 292), (5, 1_416_552_448, 293)])
+def test_workload_layouts(key, d, K):
+    wl = synth.workloads()[key]
+    assert wl.d == d and len(wl.layout) == K
+    off = 0
+    for (_, o, n, _) in wl.layout:
+        assert o == off and o % 32 == 0
+        off += n
+    flagged = [t[0] for t in wl.layout if t[3]]
+    assert flagged == (["wte"] if key == 4 else [])
+
+
+def test_bench_byte_model():
+    import bench
+    W = synth.workloads()
+    # sign mode: W*(G + 8 + 1/8) + W/8 + 8 bytes per parameter
+    b = bench.step_bytes(W[2])
+    assert abs(b / W[2].d - (8 * (2 + 8 + 1 / 8) + 8 / 8 + 8)) < 1e-3
+    # L1 mode: W*(G+4) + W*(G+8+n/8) + W*n/8 + 8
+    b = bench.step_bytes(W[3])
+    assert abs(b / W[3].d - (8 * 6 + 8 * (2 + 8 + 0.5) + 8 * 0.5 + 8)) < 1e-3
+    b = bench.step_bytes(W[5])
+    assert abs(b / W[5].d - (8 * 6 + 8 * (2 + 8 + 0.25) + 8 * 0.25 + 8)) < 1e-3

@@ -1,0 +1,285 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+The five workloads run at their full sizes, in the launch configuration the
+benchmark times; the oracle checks pieces of them (see tests/parity.py).
+Small cases cover ragged sizes, many worker counts, both gradient dtypes,
+every code width, the tie and average rules, the sync interval, exact zeros,
+the host-buffer entry point, determinism, checkpoint/resume and the error
+paths.  Sign mode must be bit-exact; L1 mode within the tolerances stated in
+tests/parity.py.
+"""
+import numpy as np
+import pytest
+
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    yield
+    torch.cuda.empty_cache()
+
+
+from communication_compressed_sign_gb300 import lioncub as lc  # noqa: E402
+
+WL = synth.workloads()
+
+
+def _names(wl, *names):
+    return parity.tensor_pieces(wl.layout, set(names))
+
+
+# ---------------------------------------------------------------------------
+# the five workloads, full size
+# ---------------------------------------------------------------------------
+
+def test_workload1_flat_1m_full():
+    wl = WL[1]
+    rep = parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), wl.steps)
+    assert rep.elements == 1_048_576
+
+
+def test_workload2_gpt2_small_sign():
+    wl = WL[2]
+    pieces = sorted(parity.chunk_pieces(wl.layout, "wte", 8, 4096, seed=2)
+                    + _names(wl, "h11.attn.c_proj.w", "h11.ln_2.w", "h11.ln_2.b", "h11.mlp.c_fc.b",
+                             "ln_f.w", "ln_f.b"), key=lambda p: p.src)
+    parity.run_parity(wl, pieces, wl.steps)
+
+
+def test_workload3_gpt2_medium_l1_n4():
+    wl = WL[3]
+    pieces = _names(wl, "wpe", "h0.ln_1.w", "h0.attn.c_attn.b", "h7.attn.c_proj.w", "h23.mlp.c_proj.b",
+                    "ln_f.w", "ln_f.b")
+    rep = parity.run_parity(wl, pieces, wl.steps)
+    print(rep)
+
+
+def test_workload4_gpt2_medium_w16_sync():
+    wl = WL[4]
+    pieces = sorted(parity.chunk_pieces(wl.layout, "wte", 16, 2048, seed=4)
+                    + _names(wl, "wpe", "h3.attn.c_proj.w", "ln_f.b"), key=lambda p: p.src)
+    assert any(p.flags for p in pieces)
+    parity.run_parity(wl, pieces, wl.steps)
+
+
+def test_workload5_xl_l1_n2():
+    wl = WL[5]
+    pieces = _names(wl, "wpe", "h0.ln_1.w", "h12.attn.c_proj.w", "ln_f.w", "ln_f.b")
+    rep = parity.run_parity(wl, pieces, wl.steps)
+    print(rep)
+
+
+# ---------------------------------------------------------------------------
+# small cases
+# ---------------------------------------------------------------------------
+
+def _small(d, W, grad="bf16", mode=0, nbits=1, layout=None, sync_interval=0, dist=None, seed=0):
+    layout = layout if layout is not None else synth.flat_layout(d)
+    if dist is None:
+        dist = ("t", 3.0, 1e-3, 0.0, 1.0) if grad == "bf16" else ("normal", 1e-3)
+    return synth.Workload(0, "small", W, layout, grad, dist, mode, nbits, 6, sync_interval=sync_interval,
+                          seed=seed)
+
+
+SMALL = [
+    # d, W, grad, mode, nbits
+    (1, 1, "f32", 0, 1), (31, 2, "bf16", 0, 1), (33, 3, "f32", 0, 1), (2047, 5, "bf16", 0, 1),
+    (2048, 16, "bf16", 0, 1), (2049, 4, "f32", 0, 1), (6005, 7, "bf16", 0, 1), (40000, 128, "bf16", 0, 1),
+    (1, 1, "bf16", 1, 2), (33, 2, "f32", 1, 4), (2047, 3, "bf16", 1, 8), (2049, 5, "bf16", 1, 2),
+    (6005, 16, "f32", 1, 4), (100003, 8, "bf16", 1, 4), (4099, 128, "bf16", 1, 8), (70001, 2, "bf16", 1, 2),
+]
+
+
+@pytest.mark.parametrize("d,W,grad,mode,nbits", SMALL)
+def test_small_ragged(d, W, grad, mode, nbits):
+    wl = _small(d, W, grad, mode, nbits, seed=d + W)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 6)
+
+
+def _multi_layout(sync=True):
+    sizes = [("emb", 320), ("w1", 2048 * 3), ("empty", 0), ("b1", 32), ("w2", 4096 + 64), ("tail", 45)]
+    out, off = [], 0
+    for name, n in sizes:
+        out.append((name, off, n, synth.SYNC_M if (sync and name == "emb") else 0))
+        off += n
+    return out
+
+
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 2), (1, 4), (1, 8)])
+@pytest.mark.parametrize("interval", [1, 3])
+def test_multi_tensor_sync(mode, nbits, interval):
+    layout = _multi_layout()
+    wl = _small(synth.layout_total(layout), 6, "bf16", mode, nbits, layout=layout, sync_interval=interval)
+    pieces = parity.tensor_pieces(layout, {n for (n, _, _, _) in layout})
+    parity.run_parity(wl, pieces, 7)
+
+
+@pytest.mark.parametrize("flags", [lc.FLAG_TIE_ALTERNATE, lc.FLAG_AVERAGE])
+@pytest.mark.parametrize("W", [2, 4, 9])
+def test_tie_and_average_rules(flags, W):
+    wl = _small(5000, W, "bf16", 0, 1, seed=W)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 5, mode_flags=flags)
+
+
+def test_tie_alternate_in_l1_mode():
+    wl = _small(5000, 4, "bf16", 1, 2)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 4, mode_flags=lc.FLAG_TIE_ALTERNATE)
+
+
+def _zero_pattern(t, i, g):
+    # every third element zero on even workers, every fifth on odd ones
+    g[:: 3 if i % 2 == 0 else 5] = 0
+
+
+def test_exact_zero_update_vectors():
+    """Zero gradients with m = 0 give c == 0 exactly, so the alternating rule
+    decides those bits (and, where every worker is zero, the vote)."""
+    wl = _small(4096 + 17, 4, "bf16", 0, 1, dist=("t", 3.0, 0.0, 0.0, 1.0))  # scale 0: all-zero gradients
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 4)
+    wl = _small(4096 + 17, 4, "bf16", 1, 4, dist=("t", 3.0, 0.0, 0.0, 1.0))
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3)
+    for mode, nbits in ((0, 1), (1, 2)):
+        wl = _small(9000 + 5, 6, "f32", mode, nbits)
+        parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 5, grad_hook=_zero_pattern)
+
+
+def test_host_buffer_entry_point():
+    wl = _small(70000, 4, "bf16", 0, 1)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True)
+    wl = _small(70000, 3, "f32", 1, 4)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True)
+
+
+# ---------------------------------------------------------------------------
+# determinism, checkpoint / resume, error paths
+# ---------------------------------------------------------------------------
+
+def _run_gpu(wl, steps, start=0, state=None, flags=0):
+    dev = torch.device("cuda", 0)
+    d, W = wl.d, wl.W
+    if state is None:
+        theta = torch.empty(d, dtype=torch.float32, device=dev)
+        synth.fill_theta_(theta, wl)
+        m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+    else:
+        theta, m = state
+    grads = [torch.empty(d, dtype=synth.grad_dtype(wl), device=dev) for _ in range(W)]
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
+                          wl.mode | flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
+                          wl.sync_interval)
+    m1 = None
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        lc.lioncub_set_step(h, start)
+        for t in range(start, start + steps):
+            for i in range(W):
+                synth.fill_grad_(grads[i], wl, t, i)
+            lc.lioncub_step(h, [g.data_ptr() for g in grads], torch.cuda.current_stream().cuda_stream)
+        assert lc.lioncub_get_step(h) == start + steps
+        if wl.mode == 1:
+            m1 = torch.empty((W, len(wl.layout)), dtype=torch.float32, device=dev)
+            lc.lioncub_debug_export(h, lc.EXPORT_M1, m1.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+    finally:
+        lc.lioncub_destroy(h)
+    return theta, m, m1
+
+
+def test_deterministic_l1():
+    """M1 and theta repeat bit for bit from run to run (fixed tiling, fixed
+    reduction order), including a tensor spanning hundreds of tiles."""
+    layout = [("a", 0, 1 << 20, 0), ("b", 1 << 20, 3 * 2048 + 64, 0), ("c", (1 << 20) + 3 * 2048 + 64, 77, 0)]
+    small = synth.Workload(0, "det", 4, layout, "bf16", WL[3].dist, 1, 4, 3)
+    a = _run_gpu(small, 3)
+    b = _run_gpu(small, 3)
+    assert torch.equal(a[2].view(torch.int32), b[2].view(torch.int32))
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+
+
+@pytest.mark.parametrize("mode,nbits,interval", [(0, 1, 2), (1, 4, 3)])
+def test_checkpoint_resume(mode, nbits, interval):
+    """10 steps straight equal 5 steps, a save of (theta, m, t), a new handle
+    restored to t = 5, and 5 more steps -- bit for bit."""
+    layout = _multi_layout()
+    wl = _small(synth.layout_total(layout), 4, "bf16", mode, nbits, layout=layout, sync_interval=interval)
+    th_a, m_a, _ = _run_gpu(wl, 10)
+    th_b, m_b, _ = _run_gpu(wl, 5)
+    saved = (th_b.clone(), [x.clone() for x in m_b])
+    th_c, m_c, _ = _run_gpu(wl, 5, start=5, state=saved)
+    assert torch.equal(th_a.view(torch.int32), th_c.view(torch.int32))
+    for x, y in zip(m_a, m_c):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_error_paths():
+    dev = torch.device("cuda", 0)
+    d, W = 4096, 2
+    h = lc.lioncub_create(d, W, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
+    try:
+        g = [torch.zeros(d, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_step(h, [x.data_ptr() for x in g])
+        assert e.value.code == lc.ERR_STATE
+        theta = torch.zeros(d + 4, dtype=torch.float32, device=dev)
+        m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_bind_state(h, theta.data_ptr() + 4, [x.data_ptr() for x in m])
+        assert e.value.code == lc.ERR_ALIGN
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_step(h, [g[0].data_ptr(), g[1].data_ptr() + 2])
+        assert e.value.code == lc.ERR_ALIGN
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_step(h, [g[0].data_ptr(), 0])
+        assert e.value.code == lc.ERR_ARG
+        assert lc.lioncub_get_step(h) == 0  # failed steps do not advance t
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_debug_export(h, lc.EXPORT_M1, theta.data_ptr())
+        assert e.value.code == lc.ERR_STATE
+        lc.lioncub_step(h, [x.data_ptr() for x in g])
+        torch.cuda.synchronize()
+        assert lc.lioncub_get_step(h) == 1
+    finally:
+        lc.lioncub_destroy(h)
+
+
+def test_empty_vector():
+    h = lc.lioncub_create(0, 3, None, 0.9, 0.99, 1e-4, 0.1, 1, 4, lc.GRAD_BF16, 1)
+    try:
+        dev = torch.device("cuda", 0)
+        buf = torch.zeros(4, dtype=torch.float32, device=dev)
+        lc.lioncub_bind_state(h, buf.data_ptr(), [buf.data_ptr()] * 3)
+        lc.lioncub_step(h, [buf.data_ptr()] * 3)
+        torch.cuda.synchronize()
+        assert lc.lioncub_get_step(h) == 1
+        assert lc.lioncub_wire_words(h) == 0
+    finally:
+        lc.lioncub_destroy(h)
+
+
+def test_profile_counts_launches():
+    wl = _small(100000, 4, "bf16", 1, 4)
+    dev = torch.device("cuda", 0)
+    theta = torch.zeros(wl.d, dtype=torch.float32, device=dev)
+    m = [torch.zeros(wl.d, dtype=torch.float32, device=dev) for _ in range(wl.W)]
+    g = [torch.ones(wl.d, dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    h = lc.lioncub_create(wl.d, wl.W, None, 0.9, 0.99, 1e-4, 0.1, 1, 4, lc.GRAD_BF16, 0)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        lc.lioncub_profile(h, 3)
+        for _ in range(5):
+            lc.lioncub_step(h, [x.data_ptr() for x in g])
+        for k in range(lc.KERNEL_COUNT):
+            ms, n = lc.lioncub_profile_read(h, k)
+            assert n == 3 and ms > 0.0
+    finally:
+        lc.lioncub_destroy(h)
