@@ -313,7 +313,7 @@ def run_gpu(args, wl: synth.Workload):
     step_gbs = ws_bytes / (ms * 1e-3) / 1e9
 
     # end to end: host gradients in, host theta out, through lioncub_step_host
-    e2e = run_e2e(args, wl, h, dev, stream)
+    e2e = None if args.no_e2e else run_e2e(args, wl, h, dev, stream)
 
     lc.lioncub_destroy(h)
     del grads, m, theta, flush_buf
@@ -445,6 +445,19 @@ def run_reference(args, wl: synth.Workload):
     }
 
 
+def truncated(wl: synth.Workload, limit: int) -> synth.Workload:
+    """The workload restricted to its leading tensors (at least one), about
+    `limit` parameters; the name records the cut."""
+    keep, total = [], 0
+    for t in wl.layout:
+        if keep and total + t[2] > limit:
+            break
+        keep.append(t)
+        total += t[2]
+    import dataclasses
+    return dataclasses.replace(wl, layout=keep, name=f"{wl.name}[first {len(keep)} tensors, {total} params]")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,11 +466,16 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(synth.workloads()))
     ap.add_argument("--impl", default="lioncub", choices=["lioncub", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--layout-limit", type=int, default=0,
+                    help="profiling aid: keep only the workload's leading tensors, about this many parameters")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "lioncub":
         print("note: warm-up raised to 3 steps", file=sys.stderr)
         args.warmup = 3
     wl = synth.workloads()[args.config]
+    if args.layout_limit:
+        wl = truncated(wl, args.layout_limit)
     res = run_reference(args, wl) if args.impl == "reference" else run_gpu(args, wl)
     if res is not None:
         print(json.dumps(res))
