@@ -260,7 +260,8 @@ def run_gpu(args, wl: synth.Workload):
     ws_bytes = step_bytes(wl)
     flush = ws_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    launches_per_step = 4 if wl.mode == 1 else 2
+    has_sync = any(t[3] for t in wl.layout) and wl.sync_interval == 1
+    launches_per_step = (4 if wl.mode == 1 else 2) + (1 if has_sync else 0)
 
     # warm-up
     for s in range(args.warmup):

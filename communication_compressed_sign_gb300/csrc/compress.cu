@@ -1,14 +1,14 @@
 // compress.cu -- per-worker compression pass of the compressed Lion step.
 //
-// One block per tile (2048 elements of one tensor), 8 consecutive elements
-// per thread.  For each worker i in turn the thread loads 8 gradients and 8
-// momenta, forms the update vector c ("Lion Cub: Minimizing Communication
-// Overhead in Distributed Lion", "What carries the argument"), emits the
-// wire bits -- a 0/1 sign with exact zeros sent as the step's alternating
-// sign, or the Eq. (1) L1 code -- and writes the worker's new momentum.  On
-// tensors whose momentum is synchronized this step the new momenta are
-// summed in worker order in registers and the mean is written to every
-// worker instead, so the sync costs no extra pass over memory.
+// 8 consecutive elements per thread.  For one worker the thread loads 8
+// gradients and 8 momenta, forms the update vector c ("Lion Cub: Minimizing
+// Communication Overhead in Distributed Lion", "What carries the argument"),
+// emits the wire bits -- a 0/1 sign with exact zeros sent as the step's
+// alternating sign, or the Eq. (1) L1 code -- and writes the worker's new
+// momentum.  Unsynchronized tiles run one block per (tile, worker).  On
+// tensors whose momentum is synchronized this step a block takes all
+// workers of its tile in order, sums their new momenta in registers and
+// writes the mean to every worker, so the sync costs no extra memory pass.
 //
 // Wire packing (LSB first): a thread's 8 elements hold 8*NB bits.  For the
 // 1-bit sign, four neighbouring lanes' bytes form one 32-bit word; for 2-bit
@@ -66,22 +66,73 @@ __device__ __forceinline__ void store_wire(uint32_t* wire_i, int64_t e0, int val
     }
 }
 
-template <typename GT, int NB>
-__global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a)
+// Per-element work of one worker on 8 elements: the wire bits of c and the
+// new momentum (left in m).
+template <int NB>
+__device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g, float* m, int valid, float inv)
 {
-    const Tile tl = a.tiles[blockIdx.x];
+    const uint64_t fmask = (NB == 8) ? 0xffull : ((1ull << NB) - 1ull);
+    uint64_t bits = 0;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
+        uint64_t field;
+        if constexpr (NB == 1)
+            field = sign_bit(c, a.zero_bit);
+        else
+            field = static_cast<uint64_t>(static_cast<uint32_t>(q1_code(c, inv, a.qmax))) & fmask;
+        if (j < valid)
+            bits |= field << (NB * j);
+        m[j] = momentum(m[j], g[j], a.beta2, a.omega2);
+    }
+    return bits;
+}
+
+// Tiles whose momentum is not synchronized this step: one block per (tile,
+// worker) -- grid (tiles, W) -- so each thread handles one worker's 8
+// elements with no loop, which keeps registers low and occupancy high.
+template <typename GT, int NB>
+__global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a, int64_t tile0)
+{
+    const Tile tl = a.tiles[tile0 + blockIdx.x];
+    const int i = blockIdx.y;
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
     const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
-    const bool sync = a.sync_now && (tl.meta & kTileSync);
+    float g[kVec], m[kVec];
+    if (valid > 0) {
+        load_grad<GT>(a.g[i], e0, valid, g);
+        load_f32(a.m[i], e0, valid, m);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            g[j] = m[j] = 0.0f;
+    }
+    float inv = 0.0f;
+    if constexpr (NB > 1)
+        inv = a.inv[static_cast<int64_t>(i) * a.K + (tl.meta & ~kTileSync)];
+    const uint64_t bits = compress8<NB>(a, g, m, valid, inv);
+    store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
+    if (valid > 0)
+        store_f32(a.m[i], e0, valid, m);
+}
+
+// Tiles of synchronized tensors on a sync step: one block per tile, the
+// thread loops over the workers in order, summing their new momenta in
+// registers, and writes the mean to every worker (no extra memory pass).
+template <typename GT, int NB>
+__global__ void __launch_bounds__(kThreads) k_compress_sync(const StepArgs a, int64_t tile0)
+{
+    const Tile tl = a.tiles[tile0 + blockIdx.x];
+    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
     const int k = static_cast<int>(tl.meta & ~kTileSync);
-    const uint64_t fmask = (NB == 8) ? 0xffull : ((1ull << NB) - 1ull);
 
     float acc[kVec];
 #pragma unroll
     for (int j = 0; j < kVec; ++j)
         acc[j] = 0.0f;
-
     for (int i = 0; i < a.W; ++i) {
         float g[kVec], m[kVec];
         if (valid > 0) {
@@ -95,32 +146,13 @@ __global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a)
         float inv = 0.0f;
         if constexpr (NB > 1)
             inv = a.inv[static_cast<int64_t>(i) * a.K + k];
-
-        uint64_t bits = 0;
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
-            uint64_t field;
-            if constexpr (NB == 1)
-                field = sign_bit(c, a.zero_bit);
-            else
-                field = static_cast<uint64_t>(static_cast<uint32_t>(q1_code(c, inv, a.qmax))) & fmask;
-            if (j < valid)
-                bits |= field << (NB * j);
-            m[j] = momentum(m[j], g[j], a.beta2, a.omega2);
-        }
+        const uint64_t bits = compress8<NB>(a, g, m, valid, inv);
         store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
-
-        if (sync) {
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
-        } else if (valid > 0) {
-            store_f32(a.m[i], e0, valid, m);
-        }
+        for (int j = 0; j < kVec; ++j)
+            acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
     }
-
-    if (sync && valid > 0) {
+    if (valid > 0) {
         const float fw = static_cast<float>(a.W);
 #pragma unroll
         for (int j = 0; j < kVec; ++j)
@@ -130,18 +162,29 @@ __global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a)
     }
 }
 
+template <typename GT, int NB>
+cudaError_t launch_nb(const StepArgs& a, cudaStream_t s)
+{
+    // Tiles [0, nplain) belong to unsynchronized tensors, [nplain, ntiles)
+    // to synchronized ones; off sync steps every tile takes the plain kernel.
+    const int64_t nplain = a.sync_now ? a.nplain : a.ntiles;
+    if (nplain > 0)
+        k_compress<GT, NB><<<dim3(static_cast<unsigned>(nplain), a.W), kThreads, 0, s>>>(a, 0);
+    if (a.ntiles > nplain)
+        k_compress_sync<GT, NB><<<static_cast<unsigned>(a.ntiles - nplain), kThreads, 0, s>>>(a, nplain);
+    return cudaGetLastError();
+}
+
 template <typename GT>
 cudaError_t launch_typed(const StepArgs& a, int nb, cudaStream_t s)
 {
-    const dim3 grid(static_cast<unsigned>(a.ntiles)), block(kThreads);
     switch (nb) {
-    case 1: k_compress<GT, 1><<<grid, block, 0, s>>>(a); break;
-    case 2: k_compress<GT, 2><<<grid, block, 0, s>>>(a); break;
-    case 4: k_compress<GT, 4><<<grid, block, 0, s>>>(a); break;
-    case 8: k_compress<GT, 8><<<grid, block, 0, s>>>(a); break;
+    case 1: return launch_nb<GT, 1>(a, s);
+    case 2: return launch_nb<GT, 2>(a, s);
+    case 4: return launch_nb<GT, 4>(a, s);
+    case 8: return launch_nb<GT, 8>(a, s);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -34,9 +34,10 @@ struct StepArgs {
     uint32_t* wire;         // W x wire_stride words (packed signs or codes)
     int64_t wire_stride;    // words per worker, a multiple of 4
     int64_t d;
-    const Tile* tiles;
+    const Tile* tiles;          // unsynchronized tensors' tiles first, then synchronized ones
     int64_t ntiles;
-    const int32_t* tile_first;  // K + 1 entries: tiles of tensor k are [tile_first[k], tile_first[k+1])
+    int64_t nplain;             // tiles of unsynchronized tensors
+    const int32_t* tile_range;  // 2K entries: tiles of tensor k are [tile_range[2k], tile_range[2k+1])
     const int64_t* numel;       // K entries
     float2* partials;           // W x ntiles compensated (hi, lo) sums of |c| (L1 mode)
     float* m1;                  // W x K (L1 mode)

@@ -37,13 +37,14 @@ struct lioncub_s {
 
     std::vector<lioncub_tensor> layout;
     int64_t ntiles = 0;
+    int64_t nplain = 0;       // tiles of unsynchronized tensors (they come first)
     int64_t wire_words = 0;   // per worker, dense
     int64_t wire_stride = 0;  // per worker, padded to 4 words
 
     // device scratch owned by the library
     uint32_t* wire = nullptr;
     Tile* tiles = nullptr;
-    int32_t* tile_first = nullptr;
+    int32_t* tile_range = nullptr;
     int64_t* numel = nullptr;
     float2* partials = nullptr;
     float* m1 = nullptr;
@@ -89,13 +90,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_scratch(lioncub_t h)
 {
-    void* ptrs[] = {h->wire, h->tiles, h->tile_first, h->numel, h->partials, h->m1, h->inv, h->staging};
+    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv, h->staging};
     for (void* p : ptrs)
         if (p)
             cudaFree(p);
     h->wire = nullptr;
     h->tiles = nullptr;
-    h->tile_first = nullptr;
+    h->tile_range = nullptr;
     h->numel = nullptr;
     h->partials = nullptr;
     h->m1 = h->inv = nullptr;
@@ -135,7 +136,8 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
     a.d = h->d;
     a.tiles = h->tiles;
     a.ntiles = h->ntiles;
-    a.tile_first = h->tile_first;
+    a.nplain = h->nplain;
+    a.tile_range = h->tile_range;
     a.numel = h->numel;
     a.partials = h->partials;
     a.m1 = h->m1;
@@ -278,25 +280,34 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
         return rc;
     }
 
-    // Tile table.
+    // Tile table: the tiles of unsynchronized tensors first, then those of
+    // synchronized tensors, so that a sync step launches each group over one
+    // contiguous range.  A tensor's tiles stay contiguous either way.
     std::vector<Tile> tiles;
-    std::vector<int32_t> first(h->K + 1, 0);
+    std::vector<int32_t> first(2 * static_cast<size_t>(h->K), 0);  // [first, end) tile range per tensor
     std::vector<int64_t> numel(h->K, 0);
-    for (int k = 0; k < h->K; ++k) {
-        const lioncub_tensor& T = h->layout[k];
-        first[k] = static_cast<int32_t>(tiles.size());
-        numel[k] = T.numel;
-        const uint32_t meta = static_cast<uint32_t>(k) | ((T.flags & LIONCUB_TENSOR_SYNC_M) ? lc::kTileSync : 0u);
-        for (int64_t s = 0; s < T.numel; s += lc::kTile) {
-            const int64_t len = (T.numel - s) < lc::kTile ? (T.numel - s) : lc::kTile;
-            tiles.push_back(Tile{T.offset + s, static_cast<int32_t>(len), meta});
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int k = 0; k < h->K; ++k) {
+            const lioncub_tensor& T = h->layout[k];
+            const bool sync = (T.flags & LIONCUB_TENSOR_SYNC_M) != 0;
+            if (sync != (pass == 1))
+                continue;
+            first[2 * k] = static_cast<int32_t>(tiles.size());
+            numel[k] = T.numel;
+            const uint32_t meta = static_cast<uint32_t>(k) | (sync ? lc::kTileSync : 0u);
+            for (int64_t s = 0; s < T.numel; s += lc::kTile) {
+                const int64_t len = (T.numel - s) < lc::kTile ? (T.numel - s) : lc::kTile;
+                tiles.push_back(Tile{T.offset + s, static_cast<int32_t>(len), meta});
+            }
+            if (tiles.size() > 0x7fffffffu) {
+                delete h;
+                return fail(nullptr, LIONCUB_ERR_ARG, "too many tiles");
+            }
+            first[2 * k + 1] = static_cast<int32_t>(tiles.size());
         }
-        if (tiles.size() > 0x7fffffffu) {
-            delete h;
-            return fail(nullptr, LIONCUB_ERR_ARG, "too many tiles");
-        }
+        if (pass == 0)
+            h->nplain = static_cast<int64_t>(tiles.size());
     }
-    first[h->K] = static_cast<int32_t>(tiles.size());
     h->ntiles = static_cast<int64_t>(tiles.size());
     h->wire_words = (d * h->nbits + 31) / 32;
     h->wire_stride = (h->wire_words + 3) / 4 * 4;
@@ -304,7 +315,7 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = dev_alloc(&h->wire, static_cast<size_t>(W) * h->wire_stride + 4);
     if (e == cudaSuccess) e = dev_alloc(&h->tiles, tiles.size());
-    if (e == cudaSuccess) e = dev_alloc(&h->tile_first, first.size());
+    if (e == cudaSuccess) e = dev_alloc(&h->tile_range, first.size());
     if (e == cudaSuccess) e = dev_alloc(&h->numel, numel.size());
     if (e == cudaSuccess && h->mode == LIONCUB_MODE_L1_INTSUM) {
         e = dev_alloc(&h->partials, static_cast<size_t>(W) * h->ntiles);
@@ -314,7 +325,7 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     if (e == cudaSuccess && !tiles.empty())
         e = cudaMemcpy(h->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
-        e = cudaMemcpy(h->tile_first, first.data(), first.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+        e = cudaMemcpy(h->tile_range, first.data(), first.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !numel.empty())
         e = cudaMemcpy(h->numel, numel.data(), numel.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)

@@ -3,18 +3,19 @@
 // Overhead in Distributed Lion", "What carries the argument": M1 is the mean
 // absolute value).
 //
-// Pass 1 (k_m1_partial): one block per tile; for each worker the block sums
-// |c| of its 2048 elements with a compensated fp32 accumulator (a hi/lo pair
-// carrying ~48 significant bits; TwoSum per element), reduced over the warp
-// with shuffles and over the 8 warps in a fixed order, and stores the (hi,
-// lo) pair.  GB300 runs fp64 at a small fraction of its fp32 rate, so a
+// Pass 1 (k_m1_partial): one block per (tile, worker) sums |c| of the tile's
+// 2048 elements with a compensated fp32 accumulator (a hi/lo pair carrying
+// ~48 significant bits; TwoSum per element), reduced over the warp with
+// shuffles and over the 8 warps in a fixed order, and stores the (hi, lo)
+// pair.  GB300 runs fp64 at a small fraction of its fp32 rate, so a
 // per-element fp64 add would cap this pass below memory speed; the pair keeps
 // the per-tile sum accurate to far below one fp32 ulp of the mean.
 //
-// Pass 2 (k_m1_finalize): one warp per (worker, tensor) sums its tiles'
-// pairs in fp64 -- lane l takes tiles l, l+32, ... in order, then a fixed
-// xor-butterfly -- divides by numel in fp64, rounds once to fp32, and stores
-// M1 and the scale inv = RN(qmax / M1) (0 when M1 == 0).
+// Pass 2 (k_m1_finalize): one block per (worker, tensor) sums its tiles'
+// pairs in fp64 -- thread t takes tiles t, t+256, ... in order, then a fixed
+// xor-butterfly per warp and the warps in order -- divides by numel in fp64,
+// rounds once to fp32, and stores M1 and the scale inv = RN(qmax / M1) (0
+// when M1 == 0).
 //
 // Both passes have fixed tilings and fixed reduction orders, so M1 is
 // bit-for-bit deterministic from run to run.
@@ -28,63 +29,70 @@ __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
 {
     __shared__ float2 red[kThreads / 32];
     const Tile tl = a.tiles[blockIdx.x];
+    const int i = blockIdx.y;
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
     const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-    for (int i = 0; i < a.W; ++i) {
-        float hi = 0.0f, lo = 0.0f;
-        if (valid > 0) {
-            float g[kVec], m[kVec];
-            load_grad<GT>(a.g[i], e0, valid, g);
-            load_f32(a.m[i], e0, valid, m);
+    float hi = 0.0f, lo = 0.0f;
+    if (valid > 0) {
+        float g[kVec], m[kVec];
+        load_grad<GT>(a.g[i], e0, valid, g);
+        load_f32(a.m[i], e0, valid, m);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (j < valid)
-                    cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
-        }
+        for (int j = 0; j < kVec; ++j)
+            if (j < valid)
+                cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
+    }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
-            const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
-            cacc_merge(hi, lo, ohi, olo);
-        }
-        if (lane == 0)
-            red[warp] = make_float2(hi, lo);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float h = red[0].x, l = red[0].y;
-            for (int w = 1; w < kThreads / 32; ++w)
-                cacc_merge(h, l, red[w].x, red[w].y);
-            a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
-        }
-        __syncthreads();
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
+        cacc_merge(hi, lo, ohi, olo);
+    }
+    if (lane == 0)
+        red[warp] = make_float2(hi, lo);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float h = red[0].x, l = red[0].y;
+        for (int w = 1; w < kThreads / 32; ++w)
+            cacc_merge(h, l, red[w].x, red[w].y);
+        a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
     }
 }
 
-__global__ void k_m1_finalize(const StepArgs a)
+// One block per (worker, tensor): thread t sums tiles t, t + 256, ... of the
+// tensor in fp64, then a fixed xor-butterfly per warp and the 8 warp sums in
+// order.
+constexpr int kFinalThreads = 256;
+
+__global__ void __launch_bounds__(kFinalThreads) k_m1_finalize(const StepArgs a)
 {
-    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= static_cast<int64_t>(a.W) * a.K)
-        return;
-    const int i = static_cast<int>(wid / a.K), k = static_cast<int>(wid % a.K);
-    const int t0 = a.tile_first[k], t1 = a.tile_first[k + 1];
+    __shared__ double red[kFinalThreads / 32];
+    const int i = blockIdx.x / a.K, k = blockIdx.x % a.K;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t0 = a.tile_range[2 * k], t1 = a.tile_range[2 * k + 1];
     const float2* p = a.partials + static_cast<int64_t>(i) * a.ntiles;
     double s = 0.0;
-    for (int t = t0 + lane; t < t1; t += 32) {
+    for (int t = t0 + threadIdx.x; t < t1; t += kFinalThreads) {
         const float2 v = p[t];
         s = __dadd_rn(s, __dadd_rn(static_cast<double>(v.x), static_cast<double>(v.y)));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
-    if (lane == 0) {
+    if (lane == 0)
+        red[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = red[0];
+        for (int w = 1; w < kFinalThreads / 32; ++w)
+            tot = __dadd_rn(tot, red[w]);
         const int64_t n = a.numel[k];
-        const float m1 = n > 0 ? __double2float_rn(__ddiv_rn(s, static_cast<double>(n))) : 0.0f;
-        a.m1[wid] = m1;
-        a.inv[wid] = m1 == 0.0f ? 0.0f : __fdiv_rn(a.qmax, m1);
+        const float m1 = n > 0 ? __double2float_rn(__ddiv_rn(tot, static_cast<double>(n))) : 0.0f;
+        a.m1[blockIdx.x] = m1;
+        a.inv[blockIdx.x] = m1 == 0.0f ? 0.0f : __fdiv_rn(a.qmax, m1);
     }
 }
 
@@ -94,7 +102,7 @@ cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s)
 {
     if (a.ntiles == 0)
         return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(a.ntiles)), block(kThreads);
+    const dim3 grid(static_cast<unsigned>(a.ntiles), a.W), block(kThreads);
     if (grad_dtype == LIONCUB_GRAD_BF16)
         k_m1_partial<__nv_bfloat16><<<grid, block, 0, s>>>(a);
     else
@@ -104,12 +112,10 @@ cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s)
 
 cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s)
 {
-    const int64_t warps = static_cast<int64_t>(a.W) * a.K;
-    if (warps == 0)
+    const int64_t blocks = static_cast<int64_t>(a.W) * a.K;
+    if (blocks == 0)
         return cudaSuccess;
-    const int block = 256;
-    const int64_t grid = (warps * 32 + block - 1) / block;
-    k_m1_finalize<<<static_cast<unsigned>(grid), block, 0, s>>>(a);
+    k_m1_finalize<<<static_cast<unsigned>(blocks), kFinalThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
