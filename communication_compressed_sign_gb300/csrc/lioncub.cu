@@ -179,6 +179,15 @@ void prof_end(lioncub_t h, int slot, cudaStream_t s)
 
 }  // namespace
 
+namespace lc {
+// Lets handle-less entry points (noalloc.cu) report a message through
+// lioncub_last_error(NULL).
+void set_handleless_error(const char* msg)
+{
+    g_create_err = msg;
+}
+}  // namespace lc
+
 extern "C" {
 
 const char* lioncub_strerror(int code)

@@ -38,8 +38,9 @@ EXPORTED = (
     "lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
     "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step", "lioncub_wire_words",
     "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read",
-    "lioncub_last_error", "lioncub_strerror", "lioncub_destroy",
+    "lioncub_last_error", "lioncub_strerror", "lioncub_destroy", "lioncub_sign_step_noalloc",
 )
+NOALLOC_MAX_WORDS = 4194304
 
 
 class LionCubError(RuntimeError):
@@ -86,6 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.lioncub_strerror.restype = ctypes.c_char_p
         L.lioncub_destroy.argtypes = [vp]
         L.lioncub_destroy.restype = None
+        L.lioncub_sign_step_noalloc.argtypes = [i64, i32, f32, f32, f32, f32, i64, i32, vp, vp, vp, vp]
+        L.lioncub_sign_step_noalloc.restype = i32
         for name in ("lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
                      "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step",
                      "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read"):
@@ -173,6 +176,15 @@ def lioncub_last_error(h) -> str:
 
 def lioncub_strerror(code: int) -> str:
     return load().lioncub_strerror(code).decode()
+
+
+def lioncub_sign_step_noalloc(d: int, W: int, beta1: float, beta2: float, lr: float, wd: float, t: int,
+                              grad_dtype: int, grad_ptrs, theta_ptr: int, m_ptrs, stream: int = 0) -> None:
+    """Handle-less sign-mode step that allocates nothing (see include/lioncub.h)."""
+    rc = load().lioncub_sign_step_noalloc(d, W, beta1, beta2, lr, wd, t, grad_dtype,
+                                          ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), theta_ptr,
+                                          ctypes.cast(_ptrs(m_ptrs), ctypes.c_void_p), stream or None)
+    _check(rc, None)
 
 
 def lioncub_destroy(h: int) -> None:

@@ -200,6 +200,37 @@ LIONCUB_API const char* lioncub_last_error(lioncub_t h);
 /* Static name of a LIONCUB_* return code. */
 LIONCUB_API const char* lioncub_strerror(int code);
 
+/*
+ * Allocation-free sign-mode step.  It has no counterpart on the pages: it is
+ * for callers that cannot allocate device memory at the time they run a step
+ * -- for example an application whose allocator has reserved all device
+ * memory up front, code that must avoid the device synchronization that
+ * cudaMalloc/cudaFree can cause, or a plug-in that may only allocate while it
+ * is initialised.  It computes the same step as lioncub_step in sign mode
+ * (one flat tensor of d elements, majority vote, ties give 0, no momentum
+ * sync) at step index t, without a handle: grads[0..W-1], theta and
+ * m[0..W-1] are the caller's device buffers (16-byte aligned), as in
+ * lioncub_bind_state / lioncub_step; the caller keeps the step counter.
+ *
+ * The packed sign words live in one array of LIONCUB_NOALLOC_MAX_WORDS
+ * uint32 (16 MiB) of the library's static device memory, which every GPU
+ * that uses this call keeps until the process exits.  Limit:
+ * W * (ceil(d/32) rounded up to a multiple of 4) <= LIONCUB_NOALLOC_MAX_WORDS
+ * (for example W = 8 and d up to 16,777,216); larger sizes return
+ * LIONCUB_ERR_ARG with a message in lioncub_last_error(NULL).  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the array: each call rewrites
+ * every word it reads, so nothing needs clearing, but calls whose kernels
+ * overlap on the GPU (other streams, other threads) race on it.  Errors:
+ * ERR_ARG, ERR_ALIGN, ERR_CUDA (messages via lioncub_last_error(NULL)).
+ */
+enum { LIONCUB_NOALLOC_MAX_WORDS = 4194304 };
+LIONCUB_API int lioncub_sign_step_noalloc(int64_t d, int W, float beta1, float beta2, float lr, float wd,
+                                          int64_t t, int grad_dtype, const void* const* grads, float* theta,
+                                          float* const* m, lioncub_stream_t stream);
+
 /* Free the handle's scratch and events.  Synchronizes the device first, so
  * no enqueued step still uses the scratch.  NULL is a no-op. */
 LIONCUB_API void lioncub_destroy(lioncub_t h);
