@@ -38,6 +38,15 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Diag(ctypes.Structure):
+    _fields_ = [("match", ctypes.c_int64), ("flip", ctypes.c_int64), ("dropped", ctypes.c_int64),
+                ("spurious", ctypes.c_int64), ("ties", ctypes.c_int64), ("max_std_m", ctypes.c_float),
+                ("pad", ctypes.c_uint32)]
+
+
+DIAG_FIELDS = ("match", "flip", "dropped", "spurious", "ties", "max_std_m")
+
+
 class Tensor(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_int64), ("numel", ctypes.c_int64), ("flags", ctypes.c_uint32)]
 
@@ -92,6 +101,12 @@ def lib() -> ctypes.CDLL:
             L.lco_step.argtypes = [i64, i32, vp, i32, f32, f32, f32, f32, i32, i32, u32, i32, i64,
                                    i32, vp, vp, vp, vp, vp, vp]
             L.lco_step.restype = i32
+            L.lco_worker_std.argtypes = [vp, i32]
+            L.lco_worker_std.restype = f32
+            L.lco_classify.argtypes = [f32, f32]
+            L.lco_classify.restype = i32
+            L.lco_diagnose.argtypes = [i64, i32, vp, i32, f32, i32, i32, u32, i64, i32, vp, vp, vp]
+            L.lco_diagnose.restype = i32
             _lib = L
     return _lib
 
@@ -241,3 +256,30 @@ def step(*, d: int, W: int, layout, beta1: float, beta2: float, lr: float, wd: f
         wire = [w[:nwords] for w in wire]
         agg = agg[:d]
     return StepOutputs(wire, m1, agg)
+
+
+# ---- diagnostics -------------------------------------------------------------
+
+def worker_std(x) -> np.float32:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return np.float32(lib().lco_worker_std(_ptr(x), x.size))
+
+
+def classify(u_q: float, u_fp: float) -> int:
+    return lib().lco_classify(u_q, u_fp)
+
+
+def diagnose(*, d: int, W: int, layout, beta1: float, mode: int, nbits: int, flags: int, t: int,
+             grads, m):
+    """Per-tensor diagnostics of one step (see lioncub_oracle.h); returns a
+    list of dicts with the DIAG_FIELDS keys."""
+    gdt = GRAD_BF16 if grads[0].dtype == np.uint16 else GRAD_F32
+    lay, K = layout_array(layout)
+    out = (Diag * max(K, 1))()
+    rc = lib().lco_diagnose(d, W, ctypes.cast(lay, ctypes.c_void_p) if lay is not None else None, K,
+                            beta1, mode, nbits, flags, t, gdt,
+                            ctypes.cast(_ptr_array(grads), ctypes.c_void_p),
+                            ctypes.cast(_ptr_array(m), ctypes.c_void_p), ctypes.addressof(out))
+    if rc != 0:
+        raise ValueError(f"oracle diagnose rejected its arguments (rc={rc})")
+    return [{f: getattr(o, f) for f in DIAG_FIELDS} for o in out]

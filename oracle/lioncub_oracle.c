@@ -319,3 +319,119 @@ done:
     free(tmpw);
     return rc;
 }
+
+/* ---- diagnostics ---------------------------------------------------------
+ * [LC] Fig. 4 / Fig. 11 captions: whether the signs of the quantized updates
+ * match or flip against the full-precision update; Fig. 6 caption: the
+ * maximum standard deviation between workers, per layer, over its elements;
+ * quoted body text: the share of tied majority votes. */
+
+float lco_worker_std(const float* x, int W)
+{
+    float s = x[0];
+    for (int i = 1; i < W; ++i)
+        s = s + x[i];
+    float mean = s / (float)W;
+    float v = 0.0f;
+    for (int i = 0; i < W; ++i) {
+        float dlt = x[i] - mean;
+        float sq = dlt * dlt;
+        v = v + sq;
+    }
+    return sqrtf(v / (float)W);
+}
+
+int lco_classify(float u_q, float u_fp)
+{
+    if (u_q == u_fp)
+        return 0;
+    if (u_q != 0.0f && u_fp != 0.0f)
+        return 1;
+    if (u_q == 0.0f)
+        return 2;
+    return 3;
+}
+
+static float sign_of(float x)
+{
+    return x > 0.0f ? 1.0f : (x < 0.0f ? -1.0f : 0.0f);
+}
+
+int lco_diagnose(int64_t d, int W, const lco_tensor* layout, int K,
+                 float beta1, int mode, int nbits, uint32_t flags, int64_t t,
+                 int grad_dtype, const void* const* grads, const float* const* m,
+                 lco_diag* out)
+{
+    if (d < 0 || W < 1 || !grads || !m || !out)
+        return -1;
+    if (mode != LCO_MODE_SIGN && mode != LCO_MODE_L1)
+        return -1;
+    if (mode == LCO_MODE_L1 && nbits != 2 && nbits != 4 && nbits != 8)
+        return -1;
+    lco_tensor whole;
+    whole.offset = 0;
+    whole.numel = d;
+    whole.flags = 0;
+    if (!layout || K == 0) {
+        layout = &whole;
+        K = 1;
+    }
+    int64_t maxn = 0;
+    for (int k = 0; k < K; ++k)
+        if (layout[k].numel > maxn)
+            maxn = layout[k].numel;
+    int rc = 0;
+    float* c = (float*)malloc((size_t)(maxn > 0 ? maxn : 1) * (size_t)W * sizeof(float));
+    int8_t* q = (int8_t*)malloc((size_t)(maxn > 0 ? maxn : 1) * (size_t)W);
+    float* col = (float*)malloc((size_t)W * sizeof(float));
+    if (!c || !q || !col) {
+        rc = -2;
+        goto done;
+    }
+    for (int k = 0; k < K; ++k) {
+        int64_t off = layout[k].offset, n = layout[k].numel;
+        lco_diag r;
+        memset(&r, 0, sizeof r);
+        /* update vectors of every worker, and their codes in L1 mode */
+        for (int i = 0; i < W; ++i) {
+            float* ci = c + (int64_t)i * n;
+            for (int64_t e = 0; e < n; ++e)
+                ci[e] = lco_update_vector(m[i][off + e], load_grad(grads[i], grad_dtype, off + e), beta1,
+                                          lco_omega(beta1));
+            if (mode == LCO_MODE_L1)
+                lco_q1(ci, n, nbits, lco_m1(ci, n), q + (int64_t)i * n);
+        }
+        for (int64_t e = 0; e < n; ++e) {
+            int32_t agg = 0;
+            float s = 0.0f;
+            for (int i = 0; i < W; ++i) {
+                float ci = c[(int64_t)i * n + e];
+                if (mode == LCO_MODE_SIGN)
+                    agg += lco_sign_bit(ci, t) ? 1 : -1;
+                else
+                    agg += q[(int64_t)i * n + e];
+                s = (i == 0) ? ci : s + ci;
+            }
+            if (agg == 0)
+                r.ties += 1;
+            float u_q = sign_of(lco_direction(agg, W, flags, t));
+            switch (lco_classify(u_q, sign_of(s))) {
+            case 0: r.match += 1; break;
+            case 1: r.flip += 1; break;
+            case 2: r.dropped += 1; break;
+            default: r.spurious += 1; break;
+            }
+            for (int i = 0; i < W; ++i)
+                col[i] = m[i][off + e];
+            float sd = lco_worker_std(col, W);
+            if (sd > r.max_std_m)
+                r.max_std_m = sd;
+        }
+        out[k] = r;
+    }
+done:
+    free(c);
+    free(q);
+    free(col);
+    return rc;
+}

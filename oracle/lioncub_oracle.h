@@ -129,6 +129,43 @@ int lco_step(int64_t d, int W, const lco_tensor* layout, int K,
              float* theta, float* const* m,
              uint32_t* const* wire_out, float* m1_out, int32_t* agg_out);
 
+/*
+ * Diagnostics of one step (the pages' own measurements), computed from the
+ * state before the step and the step's gradients; nothing is updated.
+ * Per element: u_q = sign of the update direction the step would apply
+ * (lco_direction of the method's aggregate); u_fp = sign of the full-
+ * precision sum s = c_0 + c_1 + ... + c_{W-1} (fp32, in worker order).
+ *   match:    u_q == u_fp
+ *   flip:     u_q == -u_fp != 0
+ *   dropped:  u_q == 0 != u_fp
+ *   spurious: u_fp == 0 != u_q
+ *   ties:     elements whose aggregate is exactly 0
+ * max_std_m: the largest, over the tensor's elements, inter-worker standard
+ * deviation of the momentum: mean = (sum_i m_i) / W, var = (sum_i
+ * (m_i - mean)^2) / W, both sums in worker order in fp32, std = sqrt(var).
+ * [LC] Fig. 4 / Fig. 11 captions (sign match and flip rates of quantized
+ * updates), Fig. 6 caption (maximum inter-worker standard deviation per
+ * layer), the quoted body text on tied votes.
+ */
+typedef struct {
+    int64_t match, flip, dropped, spurious, ties;
+    float max_std_m;
+    uint32_t pad;
+} lco_diag;
+
+/* Inter-worker standard deviation of values x_0..x_{W-1} (as above). */
+float lco_worker_std(const float* x, int W);
+
+/* Classify one element: returns 0 match, 1 flip, 2 dropped, 3 spurious. */
+int lco_classify(float u_q, float u_fp);
+
+/* Diagnostics for every tensor (out[k], K entries; layout NULL/K = 0 means
+ * one tensor).  Arguments as in lco_step.  Returns 0, -1 or -2 as lco_step. */
+int lco_diagnose(int64_t d, int W, const lco_tensor* layout, int K,
+                 float beta1, int mode, int nbits, uint32_t flags, int64_t t,
+                 int grad_dtype, const void* const* grads, const float* const* m,
+                 lco_diag* out);
+
 #ifdef __cplusplus
 }
 #endif

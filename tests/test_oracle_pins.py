@@ -398,3 +398,98 @@ def test_step_rejects_bad_arguments(oracle_lib):
         oracle.step(layout=[(0, 32, 0)], mode=0, nbits=1, **kw)  # does not cover d
     with pytest.raises(ValueError):
         oracle.step(layout=None, mode=1, nbits=3, **kw)
+
+
+# ---------------------------------------------------------------------------
+# Diagnostics (Fig. 4 / Fig. 11 sign match and flip, Fig. 6 momentum std,
+# tied votes)
+# ---------------------------------------------------------------------------
+
+def test_worker_std_closed_forms(oracle_lib):
+    assert oracle.worker_std([1.0, 3.0]) == 1.0
+    assert oracle.worker_std([0.0, 0.0, 0.0, 4.0]) == np.float32(math.sqrt(3.0))
+    assert oracle.worker_std([2.5]) == 0.0
+    assert oracle.worker_std([-1.0, 1.0, -1.0, 1.0]) == 1.0
+
+
+def test_classify_table(oracle_lib):
+    assert oracle.classify(1.0, 1.0) == 0 and oracle.classify(0.0, 0.0) == 0
+    assert oracle.classify(1.0, -1.0) == 1 and oracle.classify(-1.0, 1.0) == 1
+    assert oracle.classify(0.0, 1.0) == 2 and oracle.classify(0.0, -1.0) == 2
+    assert oracle.classify(1.0, 0.0) == 3
+
+
+def test_diagnose_hand_cases(oracle_lib):
+    """beta1 = 0 makes c = g exactly.  Element by element (W = 3):
+    (2, 2, 2)    votes +3, sum +6  -> match
+    (-3, 1, 1)   votes +1, sum -1  -> flip (majority disagrees with the sum)
+    (3, -1, 0)   t = 1: zero sends -1, votes -1, sum +2 -> flip
+    (1, -1, 0)   t = 1: votes -1, sum 0 -> spurious
+    and W = 2: (3, -1) votes 0 (tie), sum +2 -> dropped."""
+    g3 = [np.array(v, np.float32) for v in ([2, -3, 3, 1], [2, 1, -1, -1], [2, 1, 0, 0])]
+    m3 = [np.array([0, 0, 0, 0], np.float32), np.array([1, 0, 0, 0], np.float32),
+          np.array([3, 0, 0, 0], np.float32)]
+    r = oracle.diagnose(d=4, W=3, layout=None, beta1=0.0, mode=oracle.MODE_SIGN, nbits=1, flags=0, t=1,
+                        grads=g3, m=m3)[0]
+    assert (r["match"], r["flip"], r["dropped"], r["spurious"], r["ties"]) == (1, 2, 0, 1, 0)
+    # momentum std of element 0 over workers: values (0, 1, 3): mean 4/3
+    assert r["max_std_m"] == oracle.worker_std([0.0, 1.0, 3.0])
+    g2 = [np.array([3], np.float32), np.array([-1], np.float32)]
+    m2 = [np.zeros(1, np.float32), np.zeros(1, np.float32)]
+    r = oracle.diagnose(d=1, W=2, layout=None, beta1=0.0, mode=oracle.MODE_SIGN, nbits=1, flags=0, t=0,
+                        grads=g2, m=m2)[0]
+    assert (r["match"], r["flip"], r["dropped"], r["spurious"], r["ties"]) == (0, 0, 1, 0, 1)
+    # with the alternating tie rule the tie at even t becomes +1: a match
+    r = oracle.diagnose(d=1, W=2, layout=None, beta1=0.0, mode=oracle.MODE_SIGN, nbits=1,
+                        flags=oracle.FLAG_TIE_ALTERNATE, t=0, grads=g2, m=m2)[0]
+    assert (r["match"], r["dropped"], r["ties"]) == (1, 0, 1)
+
+
+def test_diagnose_l1_uses_q1_codes(oracle_lib):
+    """Two workers, the golden two-worker Q1 case: agg = [9,-4,-1,-1,-4,9]
+    against the full-precision sums [1001,-2,-397,296,-200,110]."""
+    g = _golden_q1()["two_workers"]
+    grads = [np.array(g["c0"], np.float32), np.array(g["c1"], np.float32)]
+    m = [np.zeros(6, np.float32), np.zeros(6, np.float32)]
+    r = oracle.diagnose(d=6, W=2, layout=None, beta1=0.0, mode=oracle.MODE_L1, nbits=4, flags=0, t=0,
+                        grads=grads, m=m)[0]
+    # signs: agg (+,-,-,-,-,+) vs sums (+,-,-,+,-,+): one flip (element 3)
+    assert (r["match"], r["flip"], r["dropped"], r["spurious"], r["ties"]) == (5, 1, 0, 0, 0)
+    assert r["max_std_m"] == 0.0
+
+
+def test_diagnose_single_worker_and_partition(oracle_lib):
+    rng = np.random.default_rng(12)
+    layout = [(0, 64, 0), (64, 96, 0), (160, 7, 0)]
+    d = 167
+    grads = [(rng.standard_normal(d) * 1e-3).astype(np.float32)]
+    m = [(rng.standard_normal(d) * 1e-3).astype(np.float32)]
+    rs = oracle.diagnose(d=d, W=1, layout=layout, beta1=0.9, mode=oracle.MODE_SIGN, nbits=1, flags=0, t=0,
+                         grads=grads, m=m)
+    for r, (_, n, _) in zip(rs, layout):
+        assert r["match"] == n and r["max_std_m"] == 0.0  # one worker: the vote is its own sign
+    W = 4
+    grads = [(rng.standard_t(3.0, d) * 1e-3).astype(np.float32) for _ in range(W)]
+    m = [(rng.standard_normal(d) * 1e-3).astype(np.float32) for _ in range(W)]
+    for mode, nbits in ((oracle.MODE_SIGN, 1), (oracle.MODE_L1, 2)):
+        rs = oracle.diagnose(d=d, W=W, layout=layout, beta1=0.9, mode=mode, nbits=nbits, flags=0, t=3,
+                             grads=grads, m=m)
+        for r, (_, n, _) in zip(rs, layout):
+            assert r["match"] + r["flip"] + r["dropped"] + r["spurious"] == n
+            assert r["ties"] >= r["dropped"]
+
+
+def test_diagnose_tie_rate_statistics(oracle_lib):
+    """Dropped updates at step 0 (m = 0, symmetric i.i.d. gradients) are the
+    tied votes: C(W, W/2) / 2^W of the elements."""
+    rng = np.random.default_rng(31)
+    d = 20000
+    for W in (4, 8):
+        grads = [(rng.standard_t(3.0, d) * 1e-3).astype(np.float32) for _ in range(W)]
+        m = [np.zeros(d, np.float32) for _ in range(W)]
+        r = oracle.diagnose(d=d, W=W, layout=None, beta1=0.9, mode=oracle.MODE_SIGN, nbits=1, flags=0, t=0,
+                            grads=grads, m=m)[0]
+        p = math.comb(W, W // 2) / 2 ** W
+        assert abs(r["ties"] / d - p) < 5 * math.sqrt(p * (1 - p) / d)
+        assert r["dropped"] == r["ties"]  # a tie is never a full-precision zero here
+        assert r["match"] > r["flip"]     # the majority usually agrees with the sum
