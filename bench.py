@@ -393,10 +393,12 @@ def run_e2e(args, wl, h, dev, stream):
     ms = reduce_max(e0.elapsed_time(e1) / args.steps, dev)
     ws, _, _ = dist_env()
     G = 4 if wl.grad == "f32" else 2
+    h2d = W * d * G
     return {"value": ws * d / (ms * 1e-3), "unit": "param-elements/s", "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / args.steps,
-            "h2d_bytes_per_step": W * d * G, "d2h_bytes_per_step": 4 * d,
-            "api": "lioncub_step_host (pinned host buffers)"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * d,
+            "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
+            "api": "lioncub_step_host (pinned host buffers; uploads overlap the previous step)"}
 
 
 def cpu_baseline(wl: synth.Workload, seconds: float = 12.0):

@@ -1,0 +1,184 @@
+// diagnose.cu -- the pages' own measurements of a compressed step, computed
+// from the state before the step and the step's gradients (nothing updated).
+//
+// "Lion Cub: Minimizing Communication Overhead in Distributed Lion":
+//   Fig. 4 / Fig. 11 captions -- whether the sign of the quantized update
+//   matches or flips against the full-precision update;
+//   Fig. 6 caption -- the maximum, over a layer's elements, of the standard
+//   deviation of the momentum between workers;
+//   quoted body text -- the share of parameters whose majority vote is tied.
+//
+// Per element: u_q is the sign of the direction the step would apply (the
+// global sign of the vote or code sum, with the tie rule); u_fp is the sign
+// of s = c_0 + c_1 + ... + c_{W-1} in fp32, worker order.  Categories: match
+// (u_q == u_fp), flip (u_q == -u_fp != 0), dropped (u_q == 0 != u_fp),
+// spurious (u_fp == 0 != u_q); ties counts aggregates equal to 0.  The
+// momentum spread is mean = (sum m_i) / W, var = (sum (m_i - mean)^2) / W,
+// std = sqrt(var), all in fp32 with one rounding per operation.
+//
+// One block per tile; each thread takes 8 elements and loops over the
+// workers (a second loop re-reads the momenta for the variance).  Per-tensor
+// totals are combined with integer atomics (exact, order-free) and the
+// maximum with an integer atomicMax on the non-negative float's bits.
+#include "device_common.cuh"
+
+namespace lc {
+namespace {
+
+template <int NB>
+__device__ __forceinline__ int wire_value(float c, float inv, float qmax, uint32_t zero_bit)
+{
+    if constexpr (NB == 1) {
+        const uint32_t b = c > 0.0f ? 1u : (c < 0.0f ? 0u : zero_bit);
+        return b ? 1 : -1;
+    } else {
+        if (inv == 0.0f)
+            return 0;
+        float r = rintf(__fmul_rn(c, inv));
+        if (r != r)
+            r = 0.0f;
+        r = fminf(fmaxf(r, -qmax), qmax);
+        return static_cast<int>(r);
+    }
+}
+
+__device__ __forceinline__ float sgn(float x)
+{
+    return x > 0.0f ? 1.0f : (x < 0.0f ? -1.0f : 0.0f);
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+template <typename GT, int NB>
+__global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub_diag* out)
+{
+    __shared__ unsigned long long red[kThreads / 32][5];
+    __shared__ float redmax[kThreads / 32];
+    const Tile tl = a.tiles[blockIdx.x];
+    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    const int k = static_cast<int>(tl.meta & ~kTileSync);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    int agg[kVec];
+    float s[kVec], ms[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        agg[j] = 0;
+        s[j] = ms[j] = 0.0f;
+    }
+    if (valid > 0) {
+        for (int i = 0; i < a.W; ++i) {
+            float g[kVec], m[kVec];
+            load_grad<GT>(a.g[i], e0, valid, g);
+            load_f32(a.m[i], e0, valid, m);
+            const float inv = (NB > 1) ? a.inv[static_cast<int64_t>(i) * a.K + k] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
+                agg[j] += wire_value<NB>(c, inv, a.qmax, a.zero_bit);
+                s[j] = (i == 0) ? c : __fadd_rn(s[j], c);
+                ms[j] = (i == 0) ? m[j] : __fadd_rn(ms[j], m[j]);
+            }
+        }
+    }
+    const float fw = static_cast<float>(a.W);
+    float var[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        ms[j] = __fdiv_rn(ms[j], fw);  // mean
+        var[j] = 0.0f;
+    }
+    if (valid > 0) {
+        for (int i = 0; i < a.W; ++i) {
+            float m[kVec];
+            load_f32(a.m[i], e0, valid, m);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float dl = __fsub_rn(m[j], ms[j]);
+                var[j] = __fadd_rn(var[j], __fmul_rn(dl, dl));
+            }
+        }
+    }
+    unsigned long long cnt[5] = {0, 0, 0, 0, 0};  // match, flip, dropped, spurious, ties
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        if (j < valid) {
+            const float uq = agg[j] > 0 ? 1.0f : (agg[j] < 0 ? -1.0f : a.tie_u);
+            const float uf = sgn(s[j]);
+            if (uq == uf)
+                cnt[0] += 1;
+            else if (uq != 0.0f && uf != 0.0f)
+                cnt[1] += 1;
+            else if (uq == 0.0f)
+                cnt[2] += 1;
+            else
+                cnt[3] += 1;
+            cnt[4] += (agg[j] == 0) ? 1 : 0;
+            mx = fmaxf(mx, __fsqrt_rn(__fdiv_rn(var[j], fw)));
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 5; ++c)
+        cnt[c] = warp_sum(cnt[c]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 5; ++c)
+            red[warp][c] = cnt[c];
+        redmax[warp] = mx;
+    }
+    __syncthreads();
+    if (threadIdx.x < 5) {
+        unsigned long long tot = 0;
+        for (int w = 0; w < kThreads / 32; ++w)
+            tot += red[w][threadIdx.x];
+        unsigned long long* base = reinterpret_cast<unsigned long long*>(&out[k]);
+        if (tot)
+            atomicAdd(base + threadIdx.x, tot);
+    } else if (threadIdx.x == 5) {
+        float m = 0.0f;
+        for (int w = 0; w < kThreads / 32; ++w)
+            m = fmaxf(m, redmax[w]);
+        atomicMax(reinterpret_cast<int*>(&out[k].max_std_m), __float_as_int(m));
+    }
+}
+
+template <typename GT>
+cudaError_t launch_typed(const StepArgs& a, int nb, lioncub_diag* out, cudaStream_t s)
+{
+    const unsigned grid = static_cast<unsigned>(a.ntiles);
+    switch (nb) {
+    case 1: k_diagnose<GT, 1><<<grid, kThreads, 0, s>>>(a, out); break;
+    case 2: k_diagnose<GT, 2><<<grid, kThreads, 0, s>>>(a, out); break;
+    case 4: k_diagnose<GT, 4><<<grid, kThreads, 0, s>>>(a, out); break;
+    case 8: k_diagnose<GT, 8><<<grid, kThreads, 0, s>>>(a, out); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lioncub_diag* out, cudaStream_t s)
+{
+    if (a.ntiles == 0)
+        return cudaSuccess;
+    const int nb = l1_mode ? a.nbits : 1;
+    if (grad_dtype == LIONCUB_GRAD_BF16)
+        return launch_typed<__nv_bfloat16>(a, nb, out, s);
+    return launch_typed<float>(a, nb, out, s);
+}
+
+}  // namespace lc

@@ -58,5 +58,6 @@ cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s)
 cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s);
 cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s);
+cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lioncub_diag* out, cudaStream_t s);
 
 }  // namespace lc

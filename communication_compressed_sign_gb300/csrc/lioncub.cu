@@ -49,11 +49,21 @@ struct lioncub_s {
     float2* partials = nullptr;
     float* m1 = nullptr;
     float* inv = nullptr;
-    // staging for lioncub_step_host
-    void* staging = nullptr;
+    // lioncub_step_host: double-buffered staging, an upload stream and the
+    // events that order uploads against the steps that read them
+    void* staging[2] = {nullptr, nullptr};
+    int nstaging = 0;
+    size_t staging_stride = 0;
+    cudaStream_t up = nullptr;
+    cudaEvent_t ev_up[2] = {nullptr, nullptr};
+    cudaEvent_t ev_used[2] = {nullptr, nullptr};
+    bool used_recorded[2] = {false, false};
+    int64_t host_calls = 0;
 
     // profiling
-    int prof_capacity = 0;  // launches that can still be recorded
+    int prof_steps_left = 0;   // steps still to record
+    bool prof_this_call = false;
+    int prof_capacity = 0;     // event-pair slots
     std::vector<cudaEvent_t> prof_events;  // pairs
     std::vector<int> prof_kernel;
     int prof_used = 0;
@@ -90,7 +100,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_scratch(lioncub_t h)
 {
-    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv, h->staging};
+    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv,
+                    h->staging[0], h->staging[1]};
     for (void* p : ptrs)
         if (p)
             cudaFree(p);
@@ -100,7 +111,18 @@ void free_scratch(lioncub_t h)
     h->numel = nullptr;
     h->partials = nullptr;
     h->m1 = h->inv = nullptr;
-    h->staging = nullptr;
+    h->staging[0] = h->staging[1] = nullptr;
+    h->nstaging = 0;
+    for (int b = 0; b < 2; ++b) {
+        if (h->ev_up[b])
+            cudaEventDestroy(h->ev_up[b]);
+        if (h->ev_used[b])
+            cudaEventDestroy(h->ev_used[b]);
+        h->ev_up[b] = h->ev_used[b] = nullptr;
+    }
+    if (h->up)
+        cudaStreamDestroy(h->up);
+    h->up = nullptr;
 }
 
 void drop_profile(lioncub_t h)
@@ -111,6 +133,8 @@ void drop_profile(lioncub_t h)
     h->prof_kernel.clear();
     h->prof_capacity = 0;
     h->prof_used = 0;
+    h->prof_steps_left = 0;
+    h->prof_this_call = false;
 }
 
 template <typename T>
@@ -163,7 +187,7 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
 // Records an event before a launch when profiling is on; returns the slot.
 int prof_begin(lioncub_t h, int kernel, cudaStream_t s)
 {
-    if (h->prof_used >= h->prof_capacity)
+    if (!h->prof_this_call || h->prof_used >= h->prof_capacity)
         return -1;
     const int slot = h->prof_used++;
     h->prof_kernel[slot] = kernel;
@@ -389,6 +413,9 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const StepArgs a = make_args(h, grads);
     const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
+    h->prof_this_call = h->prof_steps_left > 0;
+    if (h->prof_this_call)
+        --h->prof_steps_left;
     cudaError_t e;
     int slot;
     if (l1) {
@@ -426,39 +453,72 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
         return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
     if (!grads_host || !theta_host_out)
         return fail(h, LIONCUB_ERR_ARG, "grads_host and theta_host_out must be non-NULL");
-    const size_t gbytes = static_cast<size_t>(h->d) * (h->grad_dtype == LIONCUB_GRAD_BF16 ? 2 : 4);
-    const size_t gstride = (gbytes + 255) / 256 * 256;
-    if (!h->staging) {
-        cudaError_t e = cudaMalloc(&h->staging, gstride * h->W + 256);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            h->staging = nullptr;
-            return fail(h, e == cudaErrorMemoryAllocation ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA,
-                        "staging allocation of %zu bytes failed", gstride * h->W);
-        }
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const void* dev[LIONCUB_MAX_WORKERS];
-    for (int i = 0; i < h->W; ++i) {
+    for (int i = 0; i < h->W; ++i)
         if (!grads_host[i])
             return fail(h, LIONCUB_ERR_ARG, "grads_host[%d] is NULL", i);
-        char* dst = static_cast<char*>(h->staging) + gstride * i;
-        dev[i] = dst;
-        if (gbytes) {
-            cudaError_t e = cudaMemcpyAsync(dst, grads_host[i], gbytes, cudaMemcpyHostToDevice, s);
-            if (e != cudaSuccess)
-                return cuda_fail(h, e, "gradient upload");
+    const size_t gbytes = static_cast<size_t>(h->d) * (h->grad_dtype == LIONCUB_GRAD_BF16 ? 2 : 4);
+    const size_t gstride = (gbytes + 255) / 256 * 256;
+    if (h->nstaging == 0) {
+        // First call: an upload stream that never synchronizes implicitly with
+        // the legacy default stream, its events, and two staging buffers (one
+        // if memory is short, which serializes uploads behind the steps).
+        cudaError_t e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = cudaEventCreateWithFlags(&h->ev_up[b], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&h->ev_used[b], cudaEventDisableTiming);
         }
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "host-step set-up");
+        const size_t bytes = gstride * h->W + 256;
+        for (int b = 0; b < 2; ++b) {
+            e = cudaMalloc(&h->staging[b], bytes);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                h->staging[b] = nullptr;
+                break;
+            }
+            h->nstaging = b + 1;
+        }
+        if (h->nstaging == 0)
+            return fail(h, e == cudaErrorMemoryAllocation ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA,
+                        "staging allocation of %zu bytes failed", bytes);
+        h->staging_stride = gstride;
     }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int b = static_cast<int>(h->host_calls % h->nstaging);
+    cudaError_t e = cudaSuccess;
+    // The upload into buffer b waits until the step that last read b is done;
+    // it does not wait for the caller's stream, so it overlaps the previous
+    // step's kernels and its theta download.
+    if (h->used_recorded[b])
+        e = cudaStreamWaitEvent(h->up, h->ev_used[b], 0);
+    const void* dev[LIONCUB_MAX_WORKERS];
+    for (int i = 0; i < h->W && e == cudaSuccess; ++i) {
+        char* dst = static_cast<char*>(h->staging[b]) + h->staging_stride * i;
+        dev[i] = dst;
+        if (gbytes)
+            e = cudaMemcpyAsync(dst, grads_host[i], gbytes, cudaMemcpyHostToDevice, h->up);
+    }
+    if (e == cudaSuccess)
+        e = cudaEventRecord(h->ev_up[b], h->up);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(s, h->ev_up[b], 0);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "gradient upload");
     int rc = lioncub_step(h, dev, stream);
     if (rc != LIONCUB_OK)
         return rc;
-    if (h->d) {
-        cudaError_t e = cudaMemcpyAsync(theta_host_out, h->theta, static_cast<size_t>(h->d) * sizeof(float),
-                                        cudaMemcpyDeviceToHost, s);
-        if (e != cudaSuccess)
-            return cuda_fail(h, e, "theta download");
+    e = cudaEventRecord(h->ev_used[b], s);
+    if (e == cudaSuccess) {
+        h->used_recorded[b] = true;
+        if (h->d)
+            e = cudaMemcpyAsync(theta_host_out, h->theta, static_cast<size_t>(h->d) * sizeof(float),
+                                cudaMemcpyDeviceToHost, s);
     }
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "theta download");
+    ++h->host_calls;
     return LIONCUB_OK;
 }
 
@@ -527,6 +587,44 @@ int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t 
     return LIONCUB_OK;
 }
 
+int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_dev, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!h->bound)
+        return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
+    if (!grads || !out_dev)
+        return fail(h, LIONCUB_ERR_ARG, "grads and out_dev must be non-NULL");
+    if (reinterpret_cast<uintptr_t>(out_dev) & 7u)
+        return fail(h, LIONCUB_ERR_ALIGN, "out_dev is not 8-byte aligned");
+    for (int i = 0; i < h->W; ++i) {
+        if (!grads[i])
+            return fail(h, LIONCUB_ERR_ARG, "grads[%d] is NULL", i);
+        if (!aligned16(grads[i]))
+            return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const StepArgs a = make_args(h, grads);
+    const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
+    cudaError_t e = cudaMemsetAsync(out_dev, 0, static_cast<size_t>(h->K) * sizeof(lioncub_diag), s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "diagnostics reset");
+    if (l1) {
+        e = lc::launch_m1_partial(a, h->grad_dtype, s);
+        if (e == cudaSuccess)
+            e = lc::launch_m1_finalize(a, s);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "diagnostics M1 launch");
+    }
+    h->prof_this_call = h->prof_steps_left > 0;
+    const int slot = prof_begin(h, LIONCUB_KERNEL_DIAGNOSE, s);
+    e = lc::launch_diagnose(a, h->grad_dtype, l1 ? 1 : 0, out_dev, s);
+    prof_end(h, slot, s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "diagnose launch");
+    return LIONCUB_OK;
+}
+
 int lioncub_profile(lioncub_t h, int max_steps)
 {
     if (!h)
@@ -536,7 +634,8 @@ int lioncub_profile(lioncub_t h, int max_steps)
     drop_profile(h);
     if (max_steps == 0)
         return LIONCUB_OK;
-    const int launches = max_steps * LIONCUB_KERNEL_COUNT;
+    // one slot per kernel of a step, plus room for diagnose calls in between
+    const int launches = max_steps * (LIONCUB_KERNEL_COUNT + 1);
     h->prof_events.resize(2 * static_cast<size_t>(launches));
     h->prof_kernel.assign(launches, -1);
     for (size_t i = 0; i < h->prof_events.size(); ++i) {
@@ -548,6 +647,7 @@ int lioncub_profile(lioncub_t h, int max_steps)
         }
     }
     h->prof_capacity = launches;
+    h->prof_steps_left = max_steps;
     return LIONCUB_OK;
 }
 
@@ -578,7 +678,7 @@ void lioncub_destroy(lioncub_t h)
 {
     if (!h)
         return;
-    cudaDeviceSynchronize();
+    cudaDeviceSynchronize();  // no enqueued step or upload may still use the scratch
     drop_profile(h);
     free_scratch(h);
     delete h;

@@ -3,11 +3,12 @@
 // Overhead in Distributed Lion", "What carries the argument": M1 is the mean
 // absolute value).
 //
-// Pass 1 (k_m1_partial): one block per (tile, worker) sums |c| of the tile's
-// 2048 elements with a compensated fp32 accumulator (a hi/lo pair carrying
-// ~48 significant bits; TwoSum per element), reduced over the warp with
-// shuffles and over the 8 warps in a fixed order, and stores the (hi, lo)
-// pair.  GB300 runs fp64 at a small fraction of its fp32 rate, so a
+// Pass 1 (k_m1_partial): one block per tile; for each worker in turn it sums
+// |c| of the tile's 2048 elements with a compensated fp32 accumulator (a
+// hi/lo pair carrying ~48 significant bits; TwoSum per element), reduced over
+// the warp with shuffles and over the 8 warps in a fixed order, and stores
+// the (hi, lo) pair.  Looping over the workers inside the block amortizes the
+// block's start-up and its serial final merge over W tiles' worth of data.  GB300 runs fp64 at a small fraction of its fp32 rate, so a
 // per-element fp64 add would cap this pass below memory speed; the pair keeps
 // the per-tile sum accurate to far below one fp32 ulp of the mean.
 //
@@ -27,38 +28,43 @@ namespace {
 template <typename GT>
 __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
 {
-    __shared__ float2 red[kThreads / 32];
+    // Two slots alternate between consecutive workers, so one barrier per
+    // worker suffices: thread 0 has read slot (i & 1) before it reaches the
+    // barrier of worker i + 1, and slot (i & 1) is rewritten only at i + 2.
+    __shared__ float2 red[2][kThreads / 32];
     const Tile tl = a.tiles[blockIdx.x];
-    const int i = blockIdx.y;
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
     const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-    float hi = 0.0f, lo = 0.0f;
-    if (valid > 0) {
-        float g[kVec], m[kVec];
-        load_grad<GT>(a.g[i], e0, valid, g);
-        load_f32(a.m[i], e0, valid, m);
+    for (int i = 0; i < a.W; ++i) {
+        float hi = 0.0f, lo = 0.0f;
+        if (valid > 0) {
+            float g[kVec], m[kVec];
+            load_grad<GT>(a.g[i], e0, valid, g);
+            load_f32(a.m[i], e0, valid, m);
 #pragma unroll
-        for (int j = 0; j < kVec; ++j)
-            if (j < valid)
-                cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
-    }
+            for (int j = 0; j < kVec; ++j)
+                if (j < valid)
+                    cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
+        }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
-        const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
-        cacc_merge(hi, lo, ohi, olo);
-    }
-    if (lane == 0)
-        red[warp] = make_float2(hi, lo);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float h = red[0].x, l = red[0].y;
-        for (int w = 1; w < kThreads / 32; ++w)
-            cacc_merge(h, l, red[w].x, red[w].y);
-        a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+            const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
+            cacc_merge(hi, lo, ohi, olo);
+        }
+        float2* slot = red[i & 1];
+        if (lane == 0)
+            slot[warp] = make_float2(hi, lo);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float h = slot[0].x, l = slot[0].y;
+            for (int w = 1; w < kThreads / 32; ++w)
+                cacc_merge(h, l, slot[w].x, slot[w].y);
+            a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
+        }
     }
 }
 
@@ -102,7 +108,7 @@ cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s)
 {
     if (a.ntiles == 0)
         return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(a.ntiles), a.W), block(kThreads);
+    const dim3 grid(static_cast<unsigned>(a.ntiles)), block(kThreads);
     if (grad_dtype == LIONCUB_GRAD_BF16)
         k_m1_partial<__nv_bfloat16><<<grid, block, 0, s>>>(a);
     else

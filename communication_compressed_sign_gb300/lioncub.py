@@ -29,9 +29,12 @@ GRAD_F32 = 1
 OK, ERR_ARG, ERR_ALIGN, ERR_STATE, ERR_OOM, ERR_CUDA = 0, -1, -2, -3, -4, -5
 MAX_WORKERS = 128
 EXPORT_WIRE, EXPORT_M1, EXPORT_AGG = 0, 1, 2
-KERNEL_COMPRESS, KERNEL_M1, KERNEL_M1_FINAL, KERNEL_REDUCE_APPLY, KERNEL_COUNT = 0, 1, 2, 3, 4
+KERNEL_COMPRESS, KERNEL_M1, KERNEL_M1_FINAL, KERNEL_REDUCE_APPLY, KERNEL_DIAGNOSE, KERNEL_COUNT = 0, 1, 2, 3, 4, 5
 KERNEL_NAMES = {KERNEL_COMPRESS: "compress", KERNEL_M1: "m1_partial",
-                KERNEL_M1_FINAL: "m1_finalize", KERNEL_REDUCE_APPLY: "reduce_apply"}
+                KERNEL_M1_FINAL: "m1_finalize", KERNEL_REDUCE_APPLY: "reduce_apply",
+                KERNEL_DIAGNOSE: "diagnose"}
+DIAG_FIELDS = ("match", "flip", "dropped", "spurious", "ties", "max_std_m")
+DIAG_BYTES = 48
 
 # Every symbol the header declares, for load checks.
 EXPORTED = (
@@ -39,6 +42,7 @@ EXPORTED = (
     "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step", "lioncub_wire_words",
     "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read",
     "lioncub_last_error", "lioncub_strerror", "lioncub_destroy", "lioncub_sign_step_noalloc",
+    "lioncub_diagnose",
 )
 NOALLOC_MAX_WORDS = 4194304
 
@@ -89,6 +93,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.lioncub_destroy.restype = None
         L.lioncub_sign_step_noalloc.argtypes = [i64, i32, f32, f32, f32, f32, i64, i32, vp, vp, vp, vp]
         L.lioncub_sign_step_noalloc.restype = i32
+        L.lioncub_diagnose.argtypes = [vp, vp, vp, vp]
+        L.lioncub_diagnose.restype = i32
         for name in ("lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
                      "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step",
                      "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read"):
@@ -157,6 +163,21 @@ def lioncub_wire_words(h: int) -> int:
 
 def lioncub_debug_export(h: int, what: int, dst_ptr: int, stream: int = 0) -> None:
     _check(load().lioncub_debug_export(h, what, dst_ptr, stream or None), h)
+
+
+def lioncub_diagnose(h: int, grad_ptrs, out_ptr: int, stream: int = 0) -> None:
+    """Fill K lioncub_diag records (48 bytes each) at device address out_ptr."""
+    _check(load().lioncub_diagnose(h, ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), out_ptr, stream or None), h)
+
+
+def decode_diag(raw: bytes, K: int):
+    """Host bytes of K lioncub_diag records -> list of dicts."""
+    import struct
+    out = []
+    for k in range(K):
+        vals = struct.unpack_from("<5qfI", raw, k * DIAG_BYTES)
+        out.append(dict(zip(DIAG_FIELDS, vals[:6])))
+    return out
 
 
 def lioncub_profile(h: int, max_steps: int) -> None:

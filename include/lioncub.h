@@ -112,13 +112,25 @@ enum {
     LIONCUB_EXPORT_AGG = 2   /* d int32: the aggregate of the last step's wire words */
 };
 
+/* Per-tensor diagnostics of a step (lioncub_diagnose), 48 bytes. */
+typedef struct {
+    int64_t match;    /* elements whose applied sign equals the full-precision sign */
+    int64_t flip;     /* applied sign is the opposite, both non-zero                */
+    int64_t dropped;  /* applied sign 0, full-precision sign non-zero               */
+    int64_t spurious; /* applied sign non-zero, full-precision sign 0               */
+    int64_t ties;     /* elements whose aggregate is exactly 0                      */
+    float max_std_m;  /* max over the tensor of the inter-worker std of m           */
+    uint32_t reserved;
+} lioncub_diag;
+
 /* Kernels whose launches lioncub_profile_read reports. */
 enum {
     LIONCUB_KERNEL_COMPRESS = 0,     /* c, sign bits or Q1 codes, momentum, sync */
     LIONCUB_KERNEL_M1 = 1,           /* per-tile fp64 sums of |c| (L1 mode)      */
     LIONCUB_KERNEL_M1_FINAL = 2,     /* per-tensor M1 and 1/M1 scale (L1 mode)   */
     LIONCUB_KERNEL_REDUCE_APPLY = 3, /* W-way vote / integer sum, sign, theta    */
-    LIONCUB_KERNEL_COUNT = 4
+    LIONCUB_KERNEL_DIAGNOSE = 4,     /* lioncub_diagnose's counting pass          */
+    LIONCUB_KERNEL_COUNT = 5
 };
 
 /*
@@ -158,11 +170,15 @@ LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stre
 /*
  * The same step fed from host memory: copies grads_host[0..W-1] (W host
  * buffers of d gradients; page-locked memory gives full copy speed) into
- * library-owned device staging (allocated on the first call, kept until
- * destroy), runs the step, and copies the updated theta into theta_host_out
- * (d floats, host).  All copies are enqueued on `stream`; the host buffers
- * must stay valid until the stream has finished.  Errors as lioncub_step,
- * plus ERR_OOM for the staging.
+ * library-owned device staging, runs the step on `stream`, and copies the
+ * updated theta into theta_host_out (d floats, host) on `stream`.  When
+ * `stream` has completed the call's work, theta_host_out holds the result
+ * and grads_host may be reused; the host buffers must stay valid until then.
+ * The uploads run on an internal non-blocking stream into one of two staging
+ * buffers (allocated on the first call, kept until destroy; one if memory is
+ * short), so the next call's upload overlaps this call's kernels and theta
+ * download; `stream` waits for the upload before the step's kernels.
+ * Errors as lioncub_step, plus ERR_OOM for the staging.
  */
 LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
                       lioncub_stream_t stream);
@@ -185,9 +201,28 @@ LIONCUB_API int64_t lioncub_wire_words(lioncub_t h);
 LIONCUB_API int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t stream);
 
 /*
+ * The pages' own measurements for the step that `grads` would drive, from
+ * the current state; nothing is updated and the step counter does not move.
+ * "Lion Cub" Fig. 4 / Fig. 11 (whether quantized update signs match or flip
+ * against the full-precision update), Fig. 6 (maximum inter-worker standard
+ * deviation of the momentum per layer) and the share of tied majority votes.
+ * Per element, the applied sign is the sign of the direction the step would
+ * use (global sign of the vote or code sum, with the tie rule); the
+ * full-precision sign is that of s = c_0 + ... + c_{W-1} (fp32, worker
+ * order).  The momentum spread uses mean = (sum m_i)/W and var =
+ * (sum (m_i - mean)^2)/W in fp32, std = sqrt(var).  out_dev: K lioncub_diag
+ * in device memory the caller owns, zeroed and filled on `stream`.  In L1
+ * mode the M1 pass runs first and replaces the M1 that LIONCUB_EXPORT_M1
+ * returns.  Errors: ERR_STATE (unbound), ERR_ARG, ERR_ALIGN, ERR_CUDA.
+ */
+LIONCUB_API int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_dev,
+                                 lioncub_stream_t stream);
+
+/*
  * Per-kernel timing with CUDA events on the step's stream.  lioncub_profile
- * (h, n) records an event pair around every launch of the next n steps
- * (n == 0 turns recording off and drops the records).  lioncub_profile_read
+ * (h, n) records an event pair around every kernel launch of the next n
+ * lioncub_step calls (and of lioncub_diagnose calls made while steps remain
+ * to be recorded); n == 0 turns recording off and drops the records.  lioncub_profile_read
  * (synchronizes on the recorded events) gives, for one LIONCUB_KERNEL_*, the
  * summed milliseconds and the number of launches recorded.
  */

@@ -240,3 +240,57 @@ def _assert_bounds(rep: ParityReport, l1: bool, W: int, t: int):
         assert rep.theta_max_rel <= THETA_RTOL, f"step {t}: theta beyond {THETA_RTOL}: {rep}"
         assert rep.theta_mismatch_outside_agg == 0, f"step {t}: theta differs where the aggregate agreed: {rep}"
         assert rep.m_mismatch == 0, f"step {t}: momentum differs: {rep}"
+
+
+def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_flags: int = 0):
+    """Warm the state up with `warm_steps` GPU steps, then compare
+    lioncub_diagnose for the next step's gradients with the oracle's
+    diagnostics on the named whole tensors (every field exact).  Returns the
+    GPU records of those tensors."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    W, d = wl.W, wl.d
+    gdt = synth.grad_dtype(wl)
+    theta = torch.empty(d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+    grads = [torch.empty(d, dtype=gdt, device=dev) for _ in range(W)]
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
+                          wl.mode | mode_flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
+                          wl.sync_interval)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        s = torch.cuda.current_stream().cuda_stream
+        for t in range(warm_steps):
+            for i in range(W):
+                synth.fill_grad_(grads[i], wl, t, i)
+            lc.lioncub_step(h, [g.data_ptr() for g in grads], s)
+        t = warm_steps
+        for i in range(W):
+            synth.fill_grad_(grads[i], wl, t, i)
+        K = len(wl.layout)
+        out = torch.zeros(K * lc.DIAG_BYTES, dtype=torch.uint8, device=dev)
+        theta_before = theta.clone()
+        lc.lioncub_diagnose(h, [g.data_ptr() for g in grads], out.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert lc.lioncub_get_step(h) == t and torch.equal(theta, theta_before)  # nothing updated
+        gpu = lc.decode_diag(out.cpu().numpy().tobytes(), K)
+        res = []
+        for k, (name, off, n, fl) in enumerate(wl.layout):
+            if name not in tensor_names:
+                continue
+            g_o = []
+            for i in range(W):
+                gi = grads[i][off:off + n].cpu()
+                g_o.append(gi.view(torch.int16).numpy().view(np.uint16).copy() if wl.grad == "bf16"
+                           else gi.numpy().copy())
+            m_o = [x[off:off + n].cpu().numpy().copy() for x in m]
+            o = oracle.diagnose(d=n, W=W, layout=None, beta1=wl.beta1, mode=wl.mode, nbits=wl.nbits,
+                                flags=mode_flags, t=t, grads=g_o, m=m_o)[0]
+            assert gpu[k] == o, (name, gpu[k], o)
+            assert sum(gpu[k][f] for f in ("match", "flip", "dropped", "spurious")) == n
+            res.append((name, gpu[k]))
+        return res
+    finally:
+        lc.lioncub_destroy(h)

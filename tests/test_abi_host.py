@@ -32,7 +32,7 @@ def _declared():
 
 def test_header_symbols_exported(lc):
     declared = _declared()
-    assert len(declared) == 15
+    assert len(declared) == 16
     lib = ctypes.CDLL(lc.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name

@@ -278,8 +278,29 @@ def test_profile_counts_launches():
         lc.lioncub_profile(h, 3)
         for _ in range(5):
             lc.lioncub_step(h, [x.data_ptr() for x in g])
-        for k in range(lc.KERNEL_COUNT):
+        for k in (lc.KERNEL_COMPRESS, lc.KERNEL_M1, lc.KERNEL_M1_FINAL, lc.KERNEL_REDUCE_APPLY):
             ms, n = lc.lioncub_profile_read(h, k)
             assert n == 3 and ms > 0.0
+        assert lc.lioncub_profile_read(h, lc.KERNEL_DIAGNOSE) == (0.0, 0)
     finally:
         lc.lioncub_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# diagnostics (sign match / flip, ties, momentum spread)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,nbits,flags", [(0, 1, 0), (0, 1, lc.FLAG_TIE_ALTERNATE), (1, 2, 0), (1, 4, 0),
+                                              (1, 8, 0)])
+def test_diagnose_small(mode, nbits, flags):
+    layout = _multi_layout(sync=False)
+    wl = _small(synth.layout_total(layout), 6, "bf16", mode, nbits, layout=layout)
+    parity.run_diag_parity(wl, {n for (n, _, _, _) in layout}, warm_steps=3, mode_flags=flags)
+
+
+def test_diagnose_full_size_workloads():
+    for key, names in ((2, {"wpe", "h5.mlp.c_fc.b", "ln_f.w"}), (3, {"wpe", "h0.attn.c_attn.b", "ln_f.b"}),
+                       (4, {"h3.attn.c_proj.w", "ln_f.w"})):
+        res = parity.run_diag_parity(WL[key], names, warm_steps=2)
+        for name, r in res:
+            print(key, name, r)
