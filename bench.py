@@ -42,6 +42,48 @@ DEFAULT_CONFIG = 2
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
+# DRAM bytes per step of each kernel (dram__bytes_read.sum + dram__bytes_write.sum,
+# summed over the kernel's launches in one step), from one-pass ncu captures of
+# the full workloads (profiles/traffic_full_workloads.md).  Each entry holds
+# for the kernel sources it was taken on: `traffic` is reported only while the
+# fingerprint of those sources still matches.
+KERNEL_SOURCES = {
+    "compress": ("compress.cu", "device_common.cuh", "internal.h"),
+    "m1_partial": ("m1.cu", "device_common.cuh", "internal.h"),
+    "m1_finalize": ("m1.cu", "device_common.cuh", "internal.h"),
+    "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
+}
+MEASURED_TRAFFIC = {
+    "fingerprints": {"compress": "297c8b18f5e61f4e", "m1_partial": "a3515819211df8b6",
+                     "m1_finalize": "a3515819211df8b6", "reduce_apply": "90e7abe0929eaafc"},
+    "gpt2-small-124M-w8-sign": {"compress": 10019864149, "reduce_apply": 1056612181},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041380779, "m1_finalize": 11119744,
+                                 "compress": 29764140032, "reduce_apply": 4206035371},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57376469931, "reduce_apply": 3485792683},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68015030272, "m1_finalize": 44300672,
+                                  "compress": 116186189099, "reduce_apply": 14104426795},
+}
+
+
+def source_fingerprint(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "communication_compressed_sign_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per step of `kernel` on `workload`, or None when no capture
+    exists or the kernel's sources changed since it was taken."""
+    entry = MEASURED_TRAFFIC.get(workload, {})
+    if kernel not in entry or kernel not in KERNEL_SOURCES:
+        return None
+    if MEASURED_TRAFFIC["fingerprints"].get(kernel) != source_fingerprint(kernel):
+        return None
+    return entry[kernel]
+
 
 # ---------------------------------------------------------------------------
 # algorithmic bytes (every byte that must move, per parameter)
@@ -99,7 +141,7 @@ def barrier(device=None):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 50 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,7 +159,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
 
@@ -303,7 +345,7 @@ def run_gpu(args, wl: synth.Workload):
         tot, n = lc.lioncub_profile_read(h, k)
         if n:
             per_kernel[name] = {"ms_avg": tot / n, "launches": n, "share": None,
-                                "alg_bytes": kb.get(name, 0)}
+                                "alg_bytes": kb.get(name, 0), "traffic": measured_traffic(wl.name, name)}
     ksum = sum(v["ms_avg"] for v in per_kernel.values()) or 1.0
     for v in per_kernel.values():
         v["share"] = v["ms_avg"] / ksum
@@ -312,6 +354,9 @@ def run_gpu(args, wl: synth.Workload):
     peak, peak_kind = measured_hbm_peak()
     achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_avg"] * 1e-3) / 1e9
     step_gbs = ws_bytes / (ms * 1e-3) / 1e9
+
+    # diagnostics pass (not part of the step): timed separately when asked
+    diag = run_diagnose(args, wl, h, dev, stream, gptrs[0]) if args.diagnose else None
 
     # end to end: host gradients in, host theta out, through lioncub_step_host
     e2e = None if args.no_e2e else run_e2e(args, wl, h, dev, stream)
@@ -348,17 +393,75 @@ def run_gpu(args, wl: synth.Workload):
                 "frac_of_measured" if peak_kind == "measured" else "frac_of_fallback": step_gbs / peak,
                 "frac_of_nominal_7900": step_gbs / 7900.0},
         "roofline": {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": None},
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": measured_traffic(wl.name, top),
+                     "alg_bytes": per_kernel[top]["alg_bytes"]},
         "kernels": per_kernel,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
+    if diag is not None:
+        result["diagnose"] = diag
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
     if ws > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def run_diagnose(args, wl, h, dev, stream, grad_ptrs):
+    """Time lioncub_diagnose (the pages' sign match/flip, tie and momentum
+    spread measurements) over the whole workload; report its bandwidth and the
+    totals over all tensors."""
+    import torch
+    from communication_compressed_sign_gb300 import lioncub as lc
+    K = len(wl.layout)
+    out = torch.zeros(K * lc.DIAG_BYTES, dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+    for _ in range(2):
+        lc.lioncub_diagnose(h, grad_ptrs, out.data_ptr(), sp)
+    n = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        lc.lioncub_diagnose(h, grad_ptrs, out.data_ptr(), sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    recs = lc.decode_diag(out.cpu().numpy().tobytes(), K)
+    tot = {f: sum(r[f] for r in recs) for f in ("match", "flip", "dropped", "spurious", "ties")}
+    G = 4 if wl.grad == "f32" else 2
+    alg = wl.d * wl.W * (G + 4) * (2 if wl.mode == 1 else 1)  # (+ the M1 pass in L1 mode)
+    worst = max(range(K), key=lambda k: recs[k]["max_std_m"])
+    return {"ms": ms, "alg_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
+            "fractions": {f: v / wl.d for f, v in tot.items()},
+            "max_std_m": {"tensor": wl.layout[worst][0], "value": recs[worst]["max_std_m"]},
+            "state": "after the warm-up and timed steps"}
+
+
+def gpu_local_cpus(index: int):
+    """CPUs attached to GPU `index` (from its PCI device's local_cpulist), or None."""
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().lower()
+        if not bus:
+            return None
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{dom[-4:]}:{rest}/local_cpulist"
+        with open(path) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        return cpus or None
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None
 
 
 def run_e2e(args, wl, h, dev, stream):
@@ -368,6 +471,12 @@ def run_e2e(args, wl, h, dev, stream):
     from communication_compressed_sign_gb300 import lioncub as lc
     d, W = wl.d, wl.W
     gdt = synth.grad_dtype(wl)
+    # page-locked buffers on the GPU's own NUMA node: allocate (first touch)
+    # from a thread bound to the GPU's local CPUs
+    cpus = gpu_local_cpus(dev.index)
+    saved = os.sched_getaffinity(0)
+    if cpus and cpus & saved:
+        os.sched_setaffinity(0, cpus & saved)
     host = [[torch.empty(d, dtype=gdt).pin_memory() for _ in range(W)] for _ in range(2)]
     tmp = torch.empty(d, dtype=gdt, device=dev)
     for s in range(2):
@@ -394,8 +503,10 @@ def run_e2e(args, wl, h, dev, stream):
     ws, _, _ = dist_env()
     G = 4 if wl.grad == "f32" else 2
     h2d = W * d * G
+    os.sched_setaffinity(0, saved)
     return {"value": ws * d / (ms * 1e-3), "unit": "param-elements/s", "ms_per_step": ms,
             "wall_ms_per_step": wall * 1e3 / args.steps,
+            "host_cpus_bound": sorted(cpus & saved) if cpus and cpus & saved else None,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * d,
             "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
             "api": "lioncub_step_host (pinned host buffers; uploads overlap the previous step)"}
@@ -464,12 +575,14 @@ def truncated(wl: synth.Workload, limit: int) -> synth.Workload:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(synth.workloads()))
     ap.add_argument("--impl", default="lioncub", choices=["lioncub", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--diagnose", action="store_true",
+                    help="also time lioncub_diagnose (sign match/flip, ties, momentum spread)")
     ap.add_argument("--layout-limit", type=int, default=0,
                     help="profiling aid: keep only the workload's leading tensors, about this many parameters")
     args = ap.parse_args(argv)

@@ -3,7 +3,7 @@
  *
  * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded C
  * restatement of the method, used by the test suite, the smoke check and
- * the CPU-baseline leg of the benchmark to judge the CUDA library.  The
+ * the CPU-baseline leg of the benchmark to check the CUDA library.  The
  * product path never links, loads or calls it, and it shares no code,
  * header, table or helper with the CUDA library.
  *

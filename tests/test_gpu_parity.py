@@ -304,3 +304,22 @@ def test_diagnose_full_size_workloads():
         res = parity.run_diag_parity(WL[key], names, warm_steps=2)
         for name, r in res:
             print(key, name, r)
+
+
+# ---------------------------------------------------------------------------
+# beyond 32-bit element indices
+# ---------------------------------------------------------------------------
+
+def test_beyond_int32_elements():
+    """d = 2^31 + 37 elements (two tensors, the second ragged): every index in
+    the kernels is 64-bit.  Sign mode, W = 2, bf16 gradients (~30 GB on the
+    device); the oracle checks pieces at the start, across the 2^31 boundary
+    and at the ragged end."""
+    big = (1 << 31) - (1 << 20)
+    d = (1 << 31) + 37
+    layout = [("a", 0, big, 0), ("b", big, d - big, 0)]
+    wl = _small(d, 2, "bf16", 0, 1, layout=layout)
+    pieces = [parity.Piece(0, 4096, 0, -1), parity.Piece((1 << 31) - 2048, 4096, 0, -1),
+              parity.Piece(d - 101, 101, 0, -1)]
+    parity.run_parity(wl, pieces, 2)
+    torch.cuda.empty_cache()
