@@ -123,10 +123,17 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
             dst += p.n
         if l1:
             assert all(p.tensor >= 0 for p in pieces), "L1 mode needs whole-tensor pieces (M1 is per tensor)"
-        idx = torch.cat([torch.arange(p.src, p.src + p.n, device=dev) for p in pieces])
         wranges = [_words_range(p, bits) for p in pieces]
-        widx = torch.cat([torch.arange(w0, w0 + nw, device=dev) for (w0, nw) in wranges])
-        theta_o = theta[idx].cpu().numpy().copy()
+
+        # Pieces are gathered by slicing (views), never by advanced indexing:
+        # torch's gather kernel trips on tensors of more than 2^31 elements.
+        def gather(x):
+            return torch.cat([x[p.src:p.src + p.n] for p in pieces])
+
+        def gather_words(x):
+            return torch.cat([x[:, w0:w0 + nw] for (w0, nw) in wranges], dim=1)
+
+        theta_o = gather(theta).cpu().numpy().copy()
         m_o = [np.zeros(dsub, np.float32) for _ in range(W)]
         rep = ParityReport(elements=dsub)
         agg_diverged = np.zeros(dsub, bool)
@@ -145,7 +152,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
                     grad_hook(t, i, grads[i])
             g_o = []
             for i in range(W):
-                gi = grads[i][idx].cpu()
+                gi = gather(grads[i]).cpu()
                 g_o.append(gi.view(torch.int16).numpy().view(np.uint16).copy() if wl.grad == "bf16"
                            else gi.numpy().copy())
             if use_host_step:
@@ -168,8 +175,8 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
                               wd=wl.wd, mode=wl.mode, nbits=wl.nbits, flags=mode_flags,
                               sync_interval=wl.sync_interval, t=t, grads=g_o, theta=theta_o, m=m_o)
             rep.steps += 1
-            wire_h = wire[:, widx].cpu().numpy().view(np.uint32)
-            agg_h = agg[idx].cpu().numpy()
+            wire_h = gather_words(wire).cpu().numpy().view(np.uint32)
+            agg_h = gather(agg).cpu().numpy()
             agg_diff = agg_h != out.agg
             rep.agg_mismatch += int(agg_diff.sum())
             agg_diverged |= agg_diff
@@ -200,7 +207,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
                 dst += p.n
                 gsel += nw
 
-            th_g = theta[idx].cpu().numpy()
+            th_g = gather(theta).cpu().numpy()
             neq = th_g.view(np.uint32) != theta_o.view(np.uint32)
             rep.theta_mismatch = int(neq.sum())
             rep.theta_mismatch_outside_agg = int((neq & ~agg_diverged).sum())
@@ -209,7 +216,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
             rep.theta_max_rel = float(rel_ok.max()) if rel_ok.size else 0.0
             mm = 0
             for i in range(W):
-                mm += int((m[i][idx].cpu().numpy().view(np.uint32) != m_o[i].view(np.uint32)).sum())
+                mm += int((gather(m[i]).cpu().numpy().view(np.uint32) != m_o[i].view(np.uint32)).sum())
             rep.m_mismatch = mm
 
             if strict:
