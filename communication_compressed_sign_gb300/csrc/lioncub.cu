@@ -5,6 +5,7 @@
 // L1 mode (m1_partial, m1_finalize, compress, reduce_apply), all on the
 // caller's stream with no host synchronization.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -183,6 +184,15 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
     a.tie_u = (h->flags & LIONCUB_FLAG_TIE_ALTERNATE) ? (even ? 1.0f : -1.0f) : 0.0f;
     return a;
 }
+
+// NVTX range around a call or a launch (a no-op unless a tool is attached),
+// so profilers can attribute kernels to the library's steps.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Records an event before a launch when profiling is on; returns the slot.
 int prof_begin(lioncub_t h, int kernel, cudaStream_t s)
@@ -410,6 +420,7 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
         if (!aligned16(grads[i]))
             return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
     }
+    NvtxRange range("lioncub_step");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const StepArgs a = make_args(h, grads);
     const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
@@ -485,6 +496,7 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
                         "staging allocation of %zu bytes failed", bytes);
         h->staging_stride = gstride;
     }
+    NvtxRange range("lioncub_step_host");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int b = static_cast<int>(h->host_calls % h->nstaging);
     cudaError_t e = cudaSuccess;
@@ -604,6 +616,7 @@ int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_de
             return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NvtxRange range("lioncub_diagnose");
     const StepArgs a = make_args(h, grads);
     const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
     cudaError_t e = cudaMemsetAsync(out_dev, 0, static_cast<size_t>(h->K) * sizeof(lioncub_diag), s);

@@ -125,8 +125,10 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
             assert all(p.tensor >= 0 for p in pieces), "L1 mode needs whole-tensor pieces (M1 is per tensor)"
         wranges = [_words_range(p, bits) for p in pieces]
 
-        # Pieces are gathered by slicing (views), never by advanced indexing:
-        # torch's gather kernel trips on tensors of more than 2^31 elements.
+        # Pieces are gathered by slicing (views, no gather kernel).
+        for p in pieces:
+            assert 0 <= p.src and p.src + p.n <= d and p.src % 32 == 0, f"piece {p} outside [0, {d})"
+
         def gather(x):
             return torch.cat([x[p.src:p.src + p.n] for p in pieces])
 

@@ -311,15 +311,68 @@ def test_diagnose_full_size_workloads():
 # ---------------------------------------------------------------------------
 
 def test_beyond_int32_elements():
-    """d = 2^31 + 37 elements (two tensors, the second ragged): every index in
-    the kernels is 64-bit.  Sign mode, W = 2, bf16 gradients (~30 GB on the
+    """d = 2^31 + 4133 elements (two tensors, the second ragged): every index
+    in the kernels is 64-bit.  Sign mode, W = 2, bf16 gradients (~35 GB on the
     device); the oracle checks pieces at the start, across the 2^31 boundary
     and at the ragged end."""
     big = (1 << 31) - (1 << 20)
-    d = (1 << 31) + 37
+    d = (1 << 31) + 4096 + 37
     layout = [("a", 0, big, 0), ("b", big, d - big, 0)]
     wl = _small(d, 2, "bf16", 0, 1, layout=layout)
     pieces = [parity.Piece(0, 4096, 0, -1), parity.Piece((1 << 31) - 2048, 4096, 0, -1),
               parity.Piece(d - 101, 101, 0, -1)]
     parity.run_parity(wl, pieces, 2)
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# guard bands: no kernel writes outside the caller's buffers
+# ---------------------------------------------------------------------------
+
+GUARD = 64  # floats of sentinel before and after every buffer (256 bytes keeps alignment)
+
+
+def _guarded(n, dtype, fill):
+    dev = torch.device("cuda", 0)
+    buf = torch.empty(n + 2 * GUARD * (4 // torch.tensor([], dtype=dtype).element_size()), dtype=dtype, device=dev)
+    g = GUARD * (4 // buf.element_size())
+    buf.view(torch.uint8).fill_(0xA5)
+    inner = buf[g:g + n]
+    fill(inner)
+    return buf, inner, g
+
+
+@pytest.mark.parametrize("mode,nbits,d,sync", [(0, 1, 2049, 1), (0, 1, 33, 0), (1, 2, 4099, 1), (1, 8, 70001, 0)])
+def test_guard_bands_untouched(mode, nbits, d, sync):
+    W = 3
+    layout = [("a", 0, 32 * (d // 64), synth.SYNC_M if sync else 0), ("b", 32 * (d // 64), d - 32 * (d // 64), 0)]
+    wl = _small(d, W, "bf16", mode, nbits, layout=layout, sync_interval=sync)
+    tb, theta, gt = _guarded(d, torch.float32, lambda x: synth.fill_theta_(x, wl))
+    ms = [_guarded(d, torch.float32, lambda x: x.zero_()) for _ in range(W)]
+    gs = [_guarded(d, torch.bfloat16, lambda x: x.zero_()) for _ in range(W)]
+    h = lc.lioncub_create(d, W, synth.abi_layout(layout), 0.9, 0.99, 1e-4, 0.1, mode, nbits, lc.GRAD_BF16, sync)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x[1].data_ptr() for x in ms])
+        for t in range(3):
+            for i in range(W):
+                synth.fill_grad_(gs[i][1], wl, t, i)
+            lc.lioncub_step(h, [x[1].data_ptr() for x in gs], torch.cuda.current_stream().cuda_stream)
+        out = torch.empty(len(layout) * lc.DIAG_BYTES, dtype=torch.uint8, device=theta.device)
+        lc.lioncub_diagnose(h, [x[1].data_ptr() for x in gs], out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        for buf, inner, g in [(tb, theta, gt)] + ms + gs:
+            raw = buf.view(torch.uint8)
+            eb = buf.element_size()
+            assert bool((raw[: g * eb] == 0xA5).all()), "write before the buffer"
+            assert bool((raw[(g + d) * eb:] == 0xA5).all()), "write after the buffer"
+    finally:
+        lc.lioncub_destroy(h)
+
+
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 4)])
+def test_all_layer_momentum_sync(mode, nbits):
+    """Every tensor flagged: the momenta of all workers are equal after each
+    sync step (interval 2) and match the oracle."""
+    layout = [(n, o, k, synth.SYNC_M) for (n, o, k, _) in _multi_layout(sync=False)]
+    wl = _small(synth.layout_total(layout), 5, "bf16", mode, nbits, layout=layout, sync_interval=2)
+    parity.run_parity(wl, parity.tensor_pieces(layout, {n for (n, _, _, _) in layout}), 6)
