@@ -106,17 +106,6 @@ def step_bytes(wl: synth.Workload) -> int:
     return sum(kernel_bytes(wl).values())
 
 
-def compulsory_bytes(wl: synth.Workload) -> int:
-    """Bytes per step that must cross the HBM interface when the compress pass
-    re-reads the gradients and momenta from L2 (L1 mode runs M1 and compress
-    chunk by chunk): the byte model without that second read."""
-    b = step_bytes(wl)
-    if wl.mode == 1:
-        G = 4 if wl.grad == "f32" else 2
-        b -= wl.d * wl.W * (G + 4)
-    return b
-
-
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas; only the timing is reduced)
 # ---------------------------------------------------------------------------
@@ -313,6 +302,8 @@ def run_gpu(args, wl: synth.Workload):
     ws_bytes = step_bytes(wl)
     flush = ws_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    has_sync = any(t[3] for t in wl.layout) and wl.sync_interval == 1
+    launches_per_step = (4 if wl.mode == 1 else 2) + (1 if has_sync else 0)
 
     # warm-up
     for s in range(args.warmup):
@@ -350,22 +341,18 @@ def run_gpu(args, wl: synth.Workload):
 
     kb = kernel_bytes(wl)
     per_kernel = {}
-    recorded = 0
     for k, name in lc.KERNEL_NAMES.items():
         tot, n = lc.lioncub_profile_read(h, k)
-        recorded += n
         if n:
-            per_kernel[name] = {"ms_per_step": tot / args.steps, "launches_per_step": n / args.steps,
-                                "share": None, "alg_bytes": kb.get(name, 0),
-                                "traffic": measured_traffic(wl.name, name)}
-    ksum = sum(v["ms_per_step"] for v in per_kernel.values()) or 1.0
+            per_kernel[name] = {"ms_avg": tot / n, "launches": n, "share": None,
+                                "alg_bytes": kb.get(name, 0), "traffic": measured_traffic(wl.name, name)}
+    ksum = sum(v["ms_avg"] for v in per_kernel.values()) or 1.0
     for v in per_kernel.values():
-        v["share"] = v["ms_per_step"] / ksum
-        v["gbs"] = v["alg_bytes"] / (v["ms_per_step"] * 1e-3) / 1e9
+        v["share"] = v["ms_avg"] / ksum
     lc.lioncub_profile(h, 0)
-    top = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
+    top = max(per_kernel, key=lambda k: per_kernel[k]["ms_avg"])
     peak, peak_kind = measured_hbm_peak()
-    achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_per_step"] * 1e-3) / 1e9
+    achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_avg"] * 1e-3) / 1e9
     step_gbs = ws_bytes / (ms * 1e-3) / 1e9
 
     # diagnostics pass (not part of the step): timed separately when asked
@@ -402,9 +389,7 @@ def run_gpu(args, wl: synth.Workload):
             "parallelism": f"replicas x{ws} (no inter-GPU exchange)",
             "l2": "flushed between timed steps" if flush else f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB moved per step)",
         },
-        "hbm": {"alg_bytes_per_step": ws_bytes, "compulsory_bytes_per_step": compulsory_bytes(wl),
-                "achieved_gbs": step_gbs, "peak_gbs": peak,
-                "compulsory_frac": compulsory_bytes(wl) / (ms * 1e-3) / 1e9 / peak,
+        "hbm": {"alg_bytes_per_step": ws_bytes, "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac_of_measured" if peak_kind == "measured" else "frac_of_fallback": step_gbs / peak,
                 "frac_of_nominal_7900": step_gbs / 7900.0},
         "roofline": {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -412,7 +397,7 @@ def run_gpu(args, wl: synth.Workload):
                      "traffic": measured_traffic(wl.name, top),
                      "alg_bytes": per_kernel[top]["alg_bytes"]},
         "kernels": per_kernel,
-        "gpu_launches": recorded,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }

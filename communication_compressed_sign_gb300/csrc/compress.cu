@@ -175,30 +175,6 @@ cudaError_t launch_nb(const StepArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <typename GT, int NB>
-cudaError_t launch_range_nb(const StepArgs& a, int64_t tile0, int64_t n, bool sync_tiles, cudaStream_t s)
-{
-    if (n <= 0)
-        return cudaSuccess;
-    if (sync_tiles && a.sync_now)
-        k_compress_sync<GT, NB><<<static_cast<unsigned>(n), kThreads, 0, s>>>(a, tile0);
-    else
-        k_compress<GT, NB><<<dim3(static_cast<unsigned>(n), a.W), kThreads, 0, s>>>(a, tile0);
-    return cudaGetLastError();
-}
-
-template <typename GT>
-cudaError_t launch_range_typed(const StepArgs& a, int nb, int64_t tile0, int64_t n, bool sync_tiles, cudaStream_t s)
-{
-    switch (nb) {
-    case 1: return launch_range_nb<GT, 1>(a, tile0, n, sync_tiles, s);
-    case 2: return launch_range_nb<GT, 2>(a, tile0, n, sync_tiles, s);
-    case 4: return launch_range_nb<GT, 4>(a, tile0, n, sync_tiles, s);
-    case 8: return launch_range_nb<GT, 8>(a, tile0, n, sync_tiles, s);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 template <typename GT>
 cudaError_t launch_typed(const StepArgs& a, int nb, cudaStream_t s)
 {
@@ -212,15 +188,6 @@ cudaError_t launch_typed(const StepArgs& a, int nb, cudaStream_t s)
 }
 
 }  // namespace
-
-cudaError_t launch_compress_range(const StepArgs& a, int grad_dtype, int l1_mode, int64_t tile0, int64_t ntiles,
-                                  bool sync_tiles, cudaStream_t s)
-{
-    const int nb = l1_mode ? a.nbits : 1;
-    if (grad_dtype == LIONCUB_GRAD_BF16)
-        return launch_range_typed<__nv_bfloat16>(a, nb, tile0, ntiles, sync_tiles, s);
-    return launch_range_typed<float>(a, nb, tile0, ntiles, sync_tiles, s);
-}
 
 cudaError_t launch_compress(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s)
 {

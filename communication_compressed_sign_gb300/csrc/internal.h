@@ -42,7 +42,6 @@ struct StepArgs {
     float2* partials;           // W x ntiles compensated (hi, lo) sums of |c| (L1 mode)
     float* m1;                  // W x K (L1 mode)
     float* inv;                 // W x K: RN(qmax / M1), 0 where M1 == 0 (L1 mode)
-    unsigned* m1_count;         // W x K tile counters of the M1 pass, 0 between launches
     int W;
     int K;
     int nbits;
@@ -55,11 +54,8 @@ struct StepArgs {
 
 // Kernel launchers (return the launch status).
 cudaError_t launch_compress(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s);
-// compress over tiles [tile0, tile0 + ntiles), all of one kind (sync or not)
-cudaError_t launch_compress_range(const StepArgs& a, int grad_dtype, int l1_mode, int64_t tile0, int64_t ntiles,
-                                  bool sync_tiles, cudaStream_t s);
-// M1 of the tensors whose tiles are [tile0, tile0 + ntiles) (whole tensors)
-cudaError_t launch_m1(const StepArgs& a, int grad_dtype, int64_t tile0, int64_t ntiles, cudaStream_t s);
+cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s);
+cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s);
 cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s);
 cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lioncub_diag* out, cudaStream_t s);

@@ -50,14 +50,6 @@ struct lioncub_s {
     float2* partials = nullptr;
     float* m1 = nullptr;
     float* inv = nullptr;
-    unsigned* m1_count = nullptr;
-    // L1 mode: runs of whole tensors (consecutive in tile order) whose M1 and
-    // compress passes run back to back so the second read hits L2
-    struct Chunk {
-        int64_t tile0, ntiles;
-        bool sync;
-    };
-    std::vector<Chunk> chunks;
     // lioncub_step_host: double-buffered staging, an upload stream and the
     // events that order uploads against the steps that read them
     void* staging[2] = {nullptr, nullptr};
@@ -109,7 +101,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_scratch(lioncub_t h)
 {
-    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv, h->m1_count,
+    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv,
                     h->staging[0], h->staging[1]};
     for (void* p : ptrs)
         if (p)
@@ -120,7 +112,6 @@ void free_scratch(lioncub_t h)
     h->numel = nullptr;
     h->partials = nullptr;
     h->m1 = h->inv = nullptr;
-    h->m1_count = nullptr;
     h->staging[0] = h->staging[1] = nullptr;
     h->nstaging = 0;
     for (int b = 0; b < 2; ++b) {
@@ -176,7 +167,6 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
     a.partials = h->partials;
     a.m1 = h->m1;
     a.inv = h->inv;
-    a.m1_count = h->m1_count;
     a.W = h->W;
     a.K = h->K;
     a.nbits = h->nbits;
@@ -339,28 +329,12 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     std::vector<Tile> tiles;
     std::vector<int32_t> first(2 * static_cast<size_t>(h->K), 0);  // [first, end) tile range per tensor
     std::vector<int64_t> numel(h->K, 0);
-    // L1-mode chunk budget: the bytes of gradients and momenta (all workers)
-    // that one chunk may read, sized well inside the 129 MB L2.
-    int64_t budget = 64ll << 20;
-    if (const char* env = std::getenv("LIONCUB_L1_CHUNK_MB"))
-        budget = std::strtoll(env, nullptr, 10) << 20;  // 0: one chunk per tile kind
-    const int64_t gbytes = (grad_dtype == LIONCUB_GRAD_BF16) ? 2 : 4;
     for (int pass = 0; pass < 2; ++pass) {
-        int64_t chunk_bytes = 0;
-        size_t chunk_start = tiles.size();
         for (int k = 0; k < h->K; ++k) {
             const lioncub_tensor& T = h->layout[k];
             const bool sync = (T.flags & LIONCUB_TENSOR_SYNC_M) != 0;
             if (sync != (pass == 1))
                 continue;
-            const int64_t tbytes = T.numel * W * (gbytes + 4);
-            if (budget > 0 && tiles.size() > chunk_start && chunk_bytes + tbytes > budget) {
-                h->chunks.push_back({static_cast<int64_t>(chunk_start),
-                                     static_cast<int64_t>(tiles.size() - chunk_start), pass == 1});
-                chunk_start = tiles.size();
-                chunk_bytes = 0;
-            }
-            chunk_bytes += tbytes;
             first[2 * k] = static_cast<int32_t>(tiles.size());
             numel[k] = T.numel;
             const uint32_t meta = static_cast<uint32_t>(k) | (sync ? lc::kTileSync : 0u);
@@ -374,9 +348,6 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
             }
             first[2 * k + 1] = static_cast<int32_t>(tiles.size());
         }
-        if (tiles.size() > chunk_start)
-            h->chunks.push_back({static_cast<int64_t>(chunk_start),
-                                 static_cast<int64_t>(tiles.size() - chunk_start), pass == 1});
         if (pass == 0)
             h->nplain = static_cast<int64_t>(tiles.size());
     }
@@ -390,15 +361,9 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     if (e == cudaSuccess) e = dev_alloc(&h->tile_range, first.size());
     if (e == cudaSuccess) e = dev_alloc(&h->numel, numel.size());
     if (e == cudaSuccess && h->mode == LIONCUB_MODE_L1_INTSUM) {
-        const size_t wk = static_cast<size_t>(W) * h->K;
         e = dev_alloc(&h->partials, static_cast<size_t>(W) * h->ntiles);
-        if (e == cudaSuccess) e = dev_alloc(&h->m1, wk);
-        if (e == cudaSuccess) e = dev_alloc(&h->inv, wk);
-        if (e == cudaSuccess) e = dev_alloc(&h->m1_count, wk);
-        // empty tensors never get an M1 block: their M1 stays 0
-        if (e == cudaSuccess) e = cudaMemset(h->m1, 0, wk * sizeof(float));
-        if (e == cudaSuccess) e = cudaMemset(h->inv, 0, wk * sizeof(float));
-        if (e == cudaSuccess) e = cudaMemset(h->m1_count, 0, wk * sizeof(unsigned));
+        if (e == cudaSuccess) e = dev_alloc(&h->m1, static_cast<size_t>(W) * h->K);
+        if (e == cudaSuccess) e = dev_alloc(&h->inv, static_cast<size_t>(W) * h->K);
     }
     if (e == cudaSuccess && !tiles.empty())
         e = cudaMemcpy(h->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
@@ -465,27 +430,22 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
     cudaError_t e;
     int slot;
     if (l1) {
-        // chunk by chunk: M1 of the chunk's tensors, then their compression,
-        // while the chunk's gradients and momenta are still in L2
-        for (const auto& c : h->chunks) {
-            slot = prof_begin(h, LIONCUB_KERNEL_M1, s);
-            e = lc::launch_m1(a, h->grad_dtype, c.tile0, c.ntiles, s);
-            prof_end(h, slot, s);
-            if (e != cudaSuccess)
-                return cuda_fail(h, e, "m1 launch");
-            slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
-            e = lc::launch_compress_range(a, h->grad_dtype, 1, c.tile0, c.ntiles, c.sync, s);
-            prof_end(h, slot, s);
-            if (e != cudaSuccess)
-                return cuda_fail(h, e, "compress launch");
-        }
-    } else {
-        slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
-        e = lc::launch_compress(a, h->grad_dtype, 0, s);
+        slot = prof_begin(h, LIONCUB_KERNEL_M1, s);
+        e = lc::launch_m1_partial(a, h->grad_dtype, s);
         prof_end(h, slot, s);
         if (e != cudaSuccess)
-            return cuda_fail(h, e, "compress launch");
+            return cuda_fail(h, e, "m1_partial launch");
+        slot = prof_begin(h, LIONCUB_KERNEL_M1_FINAL, s);
+        e = lc::launch_m1_finalize(a, s);
+        prof_end(h, slot, s);
+        if (e != cudaSuccess)
+            return cuda_fail(h, e, "m1_finalize launch");
     }
+    slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
+    e = lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s);
+    prof_end(h, slot, s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "compress launch");
     slot = prof_begin(h, LIONCUB_KERNEL_REDUCE_APPLY, s);
     e = lc::launch_reduce_apply(a, l1 ? 1 : 0, s);
     prof_end(h, slot, s);
@@ -663,7 +623,9 @@ int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_de
     if (e != cudaSuccess)
         return cuda_fail(h, e, "diagnostics reset");
     if (l1) {
-        e = lc::launch_m1(a, h->grad_dtype, 0, h->ntiles, s);
+        e = lc::launch_m1_partial(a, h->grad_dtype, s);
+        if (e == cudaSuccess)
+            e = lc::launch_m1_finalize(a, s);
         if (e != cudaSuccess)
             return cuda_fail(h, e, "diagnostics M1 launch");
     }
@@ -685,10 +647,8 @@ int lioncub_profile(lioncub_t h, int max_steps)
     drop_profile(h);
     if (max_steps == 0)
         return LIONCUB_OK;
-    // every launch of a step (two per chunk in L1 mode), plus room for
-    // diagnose calls in between
-    const int per_step = 2 * static_cast<int>(h->chunks.size()) + LIONCUB_KERNEL_COUNT + 1;
-    const int launches = max_steps * per_step;
+    // one slot per kernel of a step, plus room for diagnose calls in between
+    const int launches = max_steps * (LIONCUB_KERNEL_COUNT + 1);
     h->prof_events.resize(2 * static_cast<size_t>(launches));
     h->prof_kernel.assign(launches, -1);
     for (size_t i = 0; i < h->prof_events.size(); ++i) {

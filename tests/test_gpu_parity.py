@@ -376,29 +376,3 @@ def test_all_layer_momentum_sync(mode, nbits):
     layout = [(n, o, k, synth.SYNC_M) for (n, o, k, _) in _multi_layout(sync=False)]
     wl = _small(synth.layout_total(layout), 5, "bf16", mode, nbits, layout=layout, sync_interval=2)
     parity.run_parity(wl, parity.tensor_pieces(layout, {n for (n, _, _, _) in layout}), 6)
-
-
-# ---------------------------------------------------------------------------
-# L1 mode runs M1 and compress chunk by chunk: the chunk budget must not
-# change a single bit
-# ---------------------------------------------------------------------------
-
-def test_l1_chunk_budget_invariance(monkeypatch):
-    sizes = [("e", 300_000), ("w1", 1_000_000), ("b1", 2048), ("w2", 700_000), ("w3", 3 * 2048), ("t", 45)]
-    layout, off = [], 0
-    for name, n in sizes:
-        layout.append((name, off, n, synth.SYNC_M if name == "w3" else 0))
-        off += n
-    wl = _small(off, 4, "bf16", 1, 4, layout=layout, sync_interval=2)
-    runs = []
-    for budget in ("0", "1", "64"):
-        monkeypatch.setenv("LIONCUB_L1_CHUNK_MB", budget)
-        runs.append(_run_gpu(wl, 4))
-    for other in runs[1:]:
-        assert torch.equal(runs[0][0].view(torch.int32), other[0].view(torch.int32))
-        assert torch.equal(runs[0][2].view(torch.int32), other[2].view(torch.int32))
-        for x, y in zip(runs[0][1], other[1]):
-            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
-    # and with many small chunks the step still matches the oracle
-    monkeypatch.setenv("LIONCUB_L1_CHUNK_MB", "1")
-    parity.run_parity(wl, parity.tensor_pieces(layout, {n for (n, _) in sizes}), 4)
