@@ -302,8 +302,6 @@ def run_gpu(args, wl: synth.Workload):
     ws_bytes = step_bytes(wl)
     flush = ws_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    has_sync = any(t[3] for t in wl.layout) and wl.sync_interval == 1
-    launches_per_step = (4 if wl.mode == 1 else 2) + (1 if has_sync else 0)
 
     # warm-up
     for s in range(args.warmup):
@@ -341,18 +339,22 @@ def run_gpu(args, wl: synth.Workload):
 
     kb = kernel_bytes(wl)
     per_kernel = {}
+    recorded = 0
     for k, name in lc.KERNEL_NAMES.items():
         tot, n = lc.lioncub_profile_read(h, k)
+        recorded += n
         if n:
-            per_kernel[name] = {"ms_avg": tot / n, "launches": n, "share": None,
-                                "alg_bytes": kb.get(name, 0), "traffic": measured_traffic(wl.name, name)}
-    ksum = sum(v["ms_avg"] for v in per_kernel.values()) or 1.0
+            per_kernel[name] = {"ms_per_step": tot / args.steps, "launches_per_step": n / args.steps,
+                                "share": None, "alg_bytes": kb.get(name, 0),
+                                "traffic": measured_traffic(wl.name, name)}
+    ksum = sum(v["ms_per_step"] for v in per_kernel.values()) or 1.0
     for v in per_kernel.values():
-        v["share"] = v["ms_avg"] / ksum
+        v["share"] = v["ms_per_step"] / ksum
+        v["gbs"] = v["alg_bytes"] / (v["ms_per_step"] * 1e-3) / 1e9
     lc.lioncub_profile(h, 0)
-    top = max(per_kernel, key=lambda k: per_kernel[k]["ms_avg"])
+    top = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
     peak, peak_kind = measured_hbm_peak()
-    achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_avg"] * 1e-3) / 1e9
+    achieved = per_kernel[top]["alg_bytes"] / (per_kernel[top]["ms_per_step"] * 1e-3) / 1e9
     step_gbs = ws_bytes / (ms * 1e-3) / 1e9
 
     # diagnostics pass (not part of the step): timed separately when asked
@@ -397,7 +399,7 @@ def run_gpu(args, wl: synth.Workload):
                      "traffic": measured_traffic(wl.name, top),
                      "alg_bytes": per_kernel[top]["alg_bytes"]},
         "kernels": per_kernel,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": recorded,
         "clocks": clk,
         "e2e": e2e,
     }
