@@ -378,7 +378,7 @@ def run_gpu(args, wl: synth.Workload):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"{'bf16' if wl.grad == 'bf16' else 'f32'} grads, f32 theta/m, u32 wire",
+        "dtype": "f32",
         "data": "synthetic (seeded counter-based Student-t / normal gradients, uniform theta)",
         "config": {
             "workload": wl.name,
@@ -387,6 +387,7 @@ def run_gpu(args, wl: synth.Workload):
             "tensors": len(wl.layout),
             "mode": "sign+majority" if wl.mode == 0 else f"L1 n={wl.nbits} + int sum",
             "grad_dtype": wl.grad,
+            "arithmetic": "f32 update vector, momentum and theta (one rounding per operation); integer vote / code sums; u32 packed wire",
             "sync": "wte every step" if wl.sync_interval else "none",
             "parallelism": f"replicas x{ws} (no inter-GPU exchange)",
             "l2": "flushed between timed steps" if flush else f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB moved per step)",
@@ -550,7 +551,7 @@ def run_reference(args, wl: synth.Workload):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 (CPU oracle), bf16 grads" if wl.grad == "bf16" else "f32 (CPU oracle)",
+        "dtype": "f32",
         "data": "synthetic (numpy Student-t / normal gradients of the workload's distribution)",
         "config": {"workload": wl.name, "workers": wl.W, "params": wl.d,
                    "sample_params": dsub, "sample_tensors": len(names)},

@@ -42,6 +42,7 @@ struct StepArgs {
     float2* partials;           // W x ntiles compensated (hi, lo) sums of |c| (L1 mode)
     float* m1;                  // W x K (L1 mode)
     float* inv;                 // W x K: RN(qmax / M1), 0 where M1 == 0 (L1 mode)
+    int* status;                // device status word: non-zero after a bounded wait gave up
     int W;
     int K;
     int nbits;

@@ -50,6 +50,7 @@ struct lioncub_s {
     float2* partials = nullptr;
     float* m1 = nullptr;
     float* inv = nullptr;
+    int* status = nullptr;  // set by a kernel whose bounded wait gave up
     // lioncub_step_host: double-buffered staging, an upload stream and the
     // events that order uploads against the steps that read them
     void* staging[2] = {nullptr, nullptr};
@@ -101,7 +102,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_scratch(lioncub_t h)
 {
-    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv,
+    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv, h->status,
                     h->staging[0], h->staging[1]};
     for (void* p : ptrs)
         if (p)
@@ -112,6 +113,7 @@ void free_scratch(lioncub_t h)
     h->numel = nullptr;
     h->partials = nullptr;
     h->m1 = h->inv = nullptr;
+    h->status = nullptr;
     h->staging[0] = h->staging[1] = nullptr;
     h->nstaging = 0;
     for (int b = 0; b < 2; ++b) {
@@ -167,6 +169,7 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
     a.partials = h->partials;
     a.m1 = h->m1;
     a.inv = h->inv;
+    a.status = h->status;
     a.W = h->W;
     a.K = h->K;
     a.nbits = h->nbits;
@@ -360,6 +363,8 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     if (e == cudaSuccess) e = dev_alloc(&h->tiles, tiles.size());
     if (e == cudaSuccess) e = dev_alloc(&h->tile_range, first.size());
     if (e == cudaSuccess) e = dev_alloc(&h->numel, numel.size());
+    if (e == cudaSuccess) e = dev_alloc(&h->status, 1);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
     if (e == cudaSuccess && h->mode == LIONCUB_MODE_L1_INTSUM) {
         e = dev_alloc(&h->partials, static_cast<size_t>(W) * h->ntiles);
         if (e == cudaSuccess) e = dev_alloc(&h->m1, static_cast<size_t>(W) * h->K);
@@ -585,6 +590,9 @@ int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t 
             return fail(h, LIONCUB_ERR_STATE, "M1 exists in L1 mode only");
         e = cudaMemcpyAsync(dst_dev, h->m1, static_cast<size_t>(h->W) * h->K * sizeof(float),
                             cudaMemcpyDeviceToDevice, s);
+        break;
+    case LIONCUB_EXPORT_STATUS:
+        e = cudaMemcpyAsync(dst_dev, h->status, sizeof(int), cudaMemcpyDeviceToDevice, s);
         break;
     case LIONCUB_EXPORT_AGG: {
         const StepArgs a = make_args(h, nullptr);

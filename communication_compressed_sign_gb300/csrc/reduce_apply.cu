@@ -130,6 +130,84 @@ __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
     store_f32(a.theta, e0, valid, th);
 }
 
+// ---- staged variant: the block's wire bytes arrive by bulk copy ------------
+//
+// One thread issues, per worker, one cp.async.bulk of the 256*NB bytes that
+// cover the block's 2048 elements (16-byte aligned: the block's byte offset
+// is a multiple of 256*NB and every worker's row is padded to 16 bytes) into
+// shared memory, completing on one mbarrier; meanwhile every thread loads its
+// theta.  The wait is bounded: if the copies have not landed after
+// kWaitLimit polls the block records an error in a.status and returns.
+
+constexpr uint32_t kWaitLimit = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+template <int NB>
+__global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
+{
+    extern __shared__ __align__(128) uint8_t rows[];  // W rows of 256*NB bytes
+    __shared__ __align__(8) uint64_t bar;
+    constexpr int kRow = 256 * NB;
+    const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * (256 * kVec);
+    const int64_t e0 = blk0 + static_cast<int64_t>(threadIdx.x) * kVec;
+    if (threadIdx.x == 0) {
+        const int64_t rem = a.d - blk0;
+        const int64_t elems = rem < 256 * kVec ? rem : 256 * kVec;
+        const uint32_t bytes = static_cast<uint32_t>(((elems * NB + 7) / 8 + 15) / 16 * 16);
+        const uint32_t b = smem_addr(&bar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes * a.W) : "memory");
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.wire) + blk0 * NB / 8;
+        const int64_t stride = a.wire_stride * 4;
+        for (int i = 0; i < a.W; ++i)
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(smem_addr(rows + i * kRow)), "l"(src + i * stride), "r"(bytes), "r"(b)
+                         : "memory");
+    }
+    const bool active = e0 < a.d;
+    const int valid = !active ? 0 : ((a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0));
+    float th[kVec];
+    if (active)
+        load_f32(a.theta, e0, valid, th);
+    __syncthreads();  // the barrier is initialised before anyone polls it
+    uint32_t ok = 0;
+    const uint32_t b = smem_addr(&bar);
+    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it)
+        asm volatile("{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0;\n selp.u32 %0, 1, 0, P;\n}"
+                     : "=r"(ok) : "r"(b) : "memory");
+    if (!ok) {
+        if (threadIdx.x == 0)
+            atomicExch(a.status, 1);
+        return;
+    }
+    if (!active)
+        return;
+    using T = typename WireChunk<NB>::T;
+    int agg[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j)
+        agg[j] = 0;
+    uint32_t lo = 0, hi = 0;
+    for (int i = 0; i < a.W; ++i)
+        accumulate<NB>(agg, lo, hi, reinterpret_cast<const T*>(rows + i * kRow)[threadIdx.x]);
+    if constexpr (NB == 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            agg[j] = 2 * static_cast<int>((lo >> (8 * j)) & 0xffu) - a.W;
+            agg[j + 4] = 2 * static_cast<int>((hi >> (8 * j)) & 0xffu) - a.W;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j)
+        th[j] = lion_apply(th[j], direction(a, agg[j]), a.lr, a.wd);
+    store_f32(a.theta, e0, valid, th);
+}
+
 template <int NB>
 __global__ void __launch_bounds__(256) k_export_agg(const StepArgs a, int32_t* out)
 {
@@ -149,6 +227,28 @@ unsigned groups_grid(int64_t d)
     return static_cast<unsigned>((groups + 255) / 256);
 }
 
+// Shared memory of the staged variant: W rows of 256*NB bytes.  Above
+// kStagedMaxBytes the register variant runs instead.
+constexpr int kStagedMaxBytes = 64 * 1024;
+
+template <int NB>
+cudaError_t launch_nb(const StepArgs& a, unsigned grid, cudaStream_t s)
+{
+    const int smem = a.W * 256 * NB;
+    if (a.status != nullptr && smem <= kStagedMaxBytes) {
+        if (smem > 48 * 1024) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(k_reduce_apply_staged<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return e;
+        }
+        k_reduce_apply_staged<NB><<<grid, 256, smem, s>>>(a);
+    } else {
+        k_reduce_apply<NB><<<grid, 256, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s)
@@ -157,13 +257,12 @@ cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s)
         return cudaSuccess;
     const unsigned grid = groups_grid(a.d);
     switch (l1_mode ? a.nbits : 1) {
-    case 1: k_reduce_apply<1><<<grid, 256, 0, s>>>(a); break;
-    case 2: k_reduce_apply<2><<<grid, 256, 0, s>>>(a); break;
-    case 4: k_reduce_apply<4><<<grid, 256, 0, s>>>(a); break;
-    case 8: k_reduce_apply<8><<<grid, 256, 0, s>>>(a); break;
+    case 1: return launch_nb<1>(a, grid, s);
+    case 2: return launch_nb<2>(a, grid, s);
+    case 4: return launch_nb<4>(a, grid, s);
+    case 8: return launch_nb<8>(a, grid, s);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s)

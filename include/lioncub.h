@@ -109,7 +109,9 @@ enum { LIONCUB_MAX_WORKERS = 128 };
 enum {
     LIONCUB_EXPORT_WIRE = 0, /* W x lioncub_wire_words() uint32: last step's packed words/codes */
     LIONCUB_EXPORT_M1 = 1,   /* W x K float: last step's M1 (L1 mode)               */
-    LIONCUB_EXPORT_AGG = 2   /* d int32: the aggregate of the last step's wire words */
+    LIONCUB_EXPORT_AGG = 2,  /* d int32: the aggregate of the last step's wire words */
+    LIONCUB_EXPORT_STATUS = 3 /* 1 int32: 0, or 1 once a kernel's bounded wait for its own
+                                 bulk copies gave up (the step's theta is then invalid) */
 };
 
 /* Per-tensor diagnostics of a step (lioncub_diagnose), 48 bytes. */
