@@ -586,6 +586,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--diagnose", action="store_true",
                     help="also time lioncub_diagnose (sign match/flip, ties, momentum spread)")
+    ap.add_argument("--mode", choices=["sign", "l1"], default=None,
+                    help="run the workload's layout and gradients with another compression mode")
+    ap.add_argument("--nbits", type=int, default=None, help="code width for --mode l1 (2, 4 or 8)")
     ap.add_argument("--layout-limit", type=int, default=0,
                     help="profiling aid: keep only the workload's leading tensors, about this many parameters")
     args = ap.parse_args(argv)
@@ -595,6 +598,12 @@ def main(argv=None):
     wl = synth.workloads()[args.config]
     if args.layout_limit:
         wl = truncated(wl, args.layout_limit)
+    if args.mode is not None:
+        import dataclasses
+        mode = 0 if args.mode == "sign" else 1
+        nbits = 1 if mode == 0 else (args.nbits or 4)
+        wl = dataclasses.replace(wl, mode=mode, nbits=nbits,
+                                 name=f"{wl.name}[{'sign' if mode == 0 else f'L1 n={nbits}'}]")
     res = run_reference(args, wl) if args.impl == "reference" else run_gpu(args, wl)
     if res is not None:
         print(json.dumps(res))

@@ -478,10 +478,14 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
         // First call: an upload stream that never synchronizes implicitly with
         // the legacy default stream, its events, and two staging buffers (one
         // if memory is short, which serializes uploads behind the steps).
-        cudaError_t e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
+        // (a retry after a failed first call creates only what is missing)
+        cudaError_t e = cudaSuccess;
+        if (!h->up)
+            e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
         for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-            e = cudaEventCreateWithFlags(&h->ev_up[b], cudaEventDisableTiming);
-            if (e == cudaSuccess)
+            if (!h->ev_up[b])
+                e = cudaEventCreateWithFlags(&h->ev_up[b], cudaEventDisableTiming);
+            if (e == cudaSuccess && !h->ev_used[b])
                 e = cudaEventCreateWithFlags(&h->ev_used[b], cudaEventDisableTiming);
         }
         if (e != cudaSuccess)

@@ -45,6 +45,9 @@
  * two's-complement n-bit codes, 32/n per word, element e in field e%(32/n)
  * of word e*n/32.  Bits past d are 0.
  *
+ * A handle is not thread-safe: calls on one handle must not overlap.  Calls
+ * on different handles may run concurrently.
+ *
  * Return codes: LIONCUB_OK (0) or a negative LIONCUB_ERR_*.  After an error,
  * lioncub_last_error(h) describes it.  Kernel faults are asynchronous: they
  * surface as LIONCUB_ERR_CUDA at a later call or at the caller's stream
