@@ -54,14 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "297c8b18f5e61f4e", "m1_partial": "a3515819211df8b6",
-                     "m1_finalize": "a3515819211df8b6", "reduce_apply": "90e7abe0929eaafc"},
-    "gpt2-small-124M-w8-sign": {"compress": 10019864149, "reduce_apply": 1056612181},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041380779, "m1_finalize": 11119744,
-                                 "compress": 29764140032, "reduce_apply": 4206035371},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57376469931, "reduce_apply": 3485792683},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68015030272, "m1_finalize": 44300672,
-                                  "compress": 116186189099, "reduce_apply": 14104426795},
+    "fingerprints": {"compress": "008d11353b94070f", "m1_partial": "23323d59e9d46bfb", "m1_finalize": "23323d59e9d46bfb", "reduce_apply": "f2b8c82ccf905d02"},
+    "gpt2-small-124M-w8-sign": {"compress": 10019691947, "reduce_apply": 1057647445},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040754688, "m1_finalize": 11119957, "compress": 29764585344, "reduce_apply": 4202920021},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57379323307, "reduce_apply": 3486156245},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68015596629, "m1_finalize": 44307627, "compress": 116185137408, "reduce_apply": 14105239595},
 }
 
 
