@@ -376,3 +376,34 @@ def test_all_layer_momentum_sync(mode, nbits):
     layout = [(n, o, k, synth.SYNC_M) for (n, o, k, _) in _multi_layout(sync=False)]
     wl = _small(synth.layout_total(layout), 5, "bf16", mode, nbits, layout=layout, sync_interval=2)
     parity.run_parity(wl, parity.tensor_pieces(layout, {n for (n, _, _, _) in layout}), 6)
+
+
+# ---------------------------------------------------------------------------
+# the torch-tensor convenience wrapper is marshalling only
+# ---------------------------------------------------------------------------
+
+def test_optimizer_wrapper_matches_c_abi():
+    from communication_compressed_sign_gb300 import LionCubOptimizer
+    layout = _multi_layout()
+    wl = _small(synth.layout_total(layout), 3, "bf16", 1, 4, layout=layout, sync_interval=2)
+    ref_theta, ref_m, _ = _run_gpu(wl, 4)
+    dev = torch.device("cuda", 0)
+    theta = torch.empty(wl.d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(wl.d, dtype=torch.float32, device=dev) for _ in range(wl.W)]
+    opt = LionCubOptimizer(wl.d, wl.W, synth.abi_layout(layout), beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr,
+                           wd=wl.wd, mode=1, nbits=4, sync_interval=2)
+    opt.bind(theta, m)
+    grads = [torch.empty(wl.d, dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    for t in range(4):
+        for i in range(wl.W):
+            synth.fill_grad_(grads[i], wl, t, i)
+        opt.step(grads)
+    torch.cuda.synchronize()
+    assert opt.t == 4
+    assert torch.equal(theta.view(torch.int32), ref_theta.view(torch.int32))
+    for x, y in zip(m, ref_m):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    with pytest.raises(ValueError):
+        opt.step(grads[:-1])
+    opt.close()
