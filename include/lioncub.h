@@ -139,6 +139,9 @@ enum {
 };
 
 /*
+ * Source: [DL] "Approach" (W workers, each with its own Lion state) and [LC]
+ * "What carries the argument" (the compression choices and the layers whose
+ * momentum is synchronized).
  * Create a handle for d parameters, W workers (1..LIONCUB_MAX_WORKERS) and a
  * layout of K tensors (layout may be NULL with K == 0: one tensor [0, d)).
  * mode: LIONCUB_MODE_* optionally OR'ed with LIONCUB_FLAG_*.  nbits: 2, 4 or
@@ -163,6 +166,10 @@ LIONCUB_API int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_t
 LIONCUB_API int lioncub_bind_state(lioncub_t h, float* theta, float* const* m);
 
 /*
+ * Source: the whole step at the top of this header -- [LC] "What carries the
+ * argument" (c, 0/1 signs with alternating zeros, Eq. (1), the quantized sum
+ * and its global sign, selective momentum sync) with textbook Lion for theta
+ * and m; [DL] "Approach" for the majority vote and the average.
  * Enqueue one step on `stream`: grads[0..W-1] are W device pointers to d
  * gradients of the handle's dtype, 16-byte aligned; the host array is read
  * during the call only, the device buffers must stay unchanged until the
@@ -188,8 +195,12 @@ LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stre
 LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
                       lioncub_stream_t stream);
 
+/* Learning rate of later steps (textbook Lion's lr). */
 LIONCUB_API int lioncub_set_lr(lioncub_t h, float lr);
-/* Step counter t (the parity of t decides the sign of an exact zero). */
+/* Step counter t (the parity of t decides the sign of an exact zero: [LC]
+ * "What carries the argument", alternating iterations).  Saving theta, the
+ * W momenta and t, then restoring them into a new handle resumes the run
+ * bit for bit. */
 LIONCUB_API int lioncub_get_step(lioncub_t h, int64_t* t);
 LIONCUB_API int lioncub_set_step(lioncub_t h, int64_t t);
 
@@ -198,6 +209,8 @@ LIONCUB_API int lioncub_set_step(lioncub_t h, int64_t t);
 LIONCUB_API int64_t lioncub_wire_words(lioncub_t h);
 
 /*
+ * Source: the wire format of [LC] "What carries the argument" and Fig. 1 /
+ * Fig. 8 captions (packed 0/1 signs, p-bit integer containers); M1 of Eq. (1).
  * Copy diagnostic data of the last step into dst_dev (device memory the
  * caller owns; sizes in the LIONCUB_EXPORT_* comments) on `stream`.  For
  * LIONCUB_EXPORT_AGG a kernel recomputes the aggregate from the wire words.

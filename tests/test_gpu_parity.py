@@ -407,3 +407,20 @@ def test_optimizer_wrapper_matches_c_abi():
     with pytest.raises(ValueError):
         opt.step(grads[:-1])
     opt.close()
+
+
+def test_create_out_of_memory_leaks_nothing():
+    """A layout whose wire buffer cannot fit (W = 128 workers of 2^35
+    elements: 512 GB of packed signs) fails with LIONCUB_ERR_OOM and leaves
+    device memory as it was."""
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    with pytest.raises(lc.LionCubError) as e:
+        lc.lioncub_create(1 << 35, 128, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
+    assert e.value.code == lc.ERR_OOM
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert abs(free1 - free0) < (64 << 20)
+    # the library is still usable afterwards
+    h = lc.lioncub_create(4096, 2, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
+    lc.lioncub_destroy(h)
