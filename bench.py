@@ -529,7 +529,7 @@ def run_reference(args, wl: synth.Workload):
     if rank != 0:
         return None
     rate = oracle_rate_probe(wl)
-    budget_s = 150.0
+    budget_s = args.ref_seconds
     per_step = budget_s / max(1, args.steps + args.warmup)
     target = int(min(wl.d, max(50_000, per_step / max(rate, 1e-12))))
     dsub, names, times = time_oracle_steps(wl, target, args.steps, args.warmup)
@@ -581,6 +581,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="lioncub", choices=["lioncub", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: CPU seconds the whole run aims at (sets the sample size)")
     ap.add_argument("--diagnose", action="store_true",
                     help="also time lioncub_diagnose (sign match/flip, ties, momentum spread)")
     ap.add_argument("--mode", choices=["sign", "l1"], default=None,

@@ -1,0 +1,36 @@
+"""The benchmark's reference arm (the CPU oracle on a bounded sample of the
+workload) runs without a GPU: check its JSON line against the contract."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "1",
+                        "--ref-seconds", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "WORLD_SIZE": "1", "RANK": "0"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference"
+    assert out["steps"] == 2 and out["warmup"] == 1 and out["higher_is_better"] is True
+    assert out["value"] > 0 and out["unit"] == "param-elements/s"
+    assert out["config"]["workload"] == "gpt2-small-124M-w8-sign"
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == out["value"] and cb["sample"]
+    assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+                        "--ref-seconds", "1"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
