@@ -26,16 +26,14 @@ __device__ __forceinline__ uint32_t sign_bit(float c, uint32_t zero_bit)
 }
 
 // Eq. (1) code of c with the per-(worker, tensor) scale inv = RN(qmax / M1):
-// round half to even, a NaN product reads as 0, clamp to [-qmax, qmax].
-__device__ __forceinline__ int q1_code(float c, float inv, float qmax)
+// y = RN(c * inv), rounded to the nearest integer with ties to even and
+// clamped to [-qmax, qmax].  The conversion instruction rounds half to even,
+// turns NaN into 0 and saturates out-of-range values, so clamping the integer
+// equals clamping rint(y); inv == 0 (M1 == 0) gives y = 0 and code 0.
+__device__ __forceinline__ int q1_code(float c, float inv, int qmax)
 {
-    if (inv == 0.0f)
-        return 0;  // M1 == 0: the whole tensor is zero
-    float r = rintf(__fmul_rn(c, inv));
-    if (r != r)
-        r = 0.0f;
-    r = fminf(fmaxf(r, -qmax), qmax);
-    return static_cast<int>(r);
+    const int r = __float2int_rn(__fmul_rn(c, inv));
+    return min(max(r, -qmax), qmax);
 }
 
 // Write this thread's 8*NB wire bits (in `bits`, low bits first) of the tile
@@ -72,6 +70,7 @@ template <int NB>
 __device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g, float* m, int valid, float inv)
 {
     const uint64_t fmask = (NB == 8) ? 0xffull : ((1ull << NB) - 1ull);
+    const int qmax_i = (1 << (NB - 1)) - 1;
     uint64_t bits = 0;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
@@ -80,7 +79,7 @@ __device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g,
         if constexpr (NB == 1)
             field = sign_bit(c, a.zero_bit);
         else
-            field = static_cast<uint64_t>(static_cast<uint32_t>(q1_code(c, inv, a.qmax))) & fmask;
+            field = static_cast<uint64_t>(static_cast<uint32_t>(q1_code(c, inv, qmax_i))) & fmask;
         if (j < valid)
             bits |= field << (NB * j);
         m[j] = momentum(m[j], g[j], a.beta2, a.omega2);
@@ -90,9 +89,10 @@ __device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g,
 
 // Tiles whose momentum is not synchronized this step: one block per (tile,
 // worker) -- grid (tiles, W) -- so each thread handles one worker's 8
-// elements with no loop, which keeps registers low and occupancy high.
+// elements with no loop, which keeps registers low: 8 blocks of 256 threads
+// per SM (at most 32 registers), the full 2048 threads.
 template <typename GT, int NB>
-__global__ void __launch_bounds__(kThreads) k_compress(const StepArgs a, int64_t tile0)
+__global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int64_t tile0)
 {
     const Tile tl = a.tiles[tile0 + blockIdx.x];
     const int i = blockIdx.y;

@@ -32,13 +32,10 @@ __device__ __forceinline__ int wire_value(float c, float inv, float qmax, uint32
         const uint32_t b = c > 0.0f ? 1u : (c < 0.0f ? 0u : zero_bit);
         return b ? 1 : -1;
     } else {
-        if (inv == 0.0f)
-            return 0;
-        float r = rintf(__fmul_rn(c, inv));
-        if (r != r)
-            r = 0.0f;
-        r = fminf(fmaxf(r, -qmax), qmax);
-        return static_cast<int>(r);
+        // nearest with ties to even; NaN gives 0; saturating, then clamped
+        const int r = __float2int_rn(__fmul_rn(c, inv));
+        const int q = static_cast<int>(qmax);
+        return min(max(r, -q), q);
     }
 }
 
