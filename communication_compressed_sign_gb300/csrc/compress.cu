@@ -101,8 +101,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int6
     const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
     float g[kVec], m[kVec];
     if (valid > 0) {
-        load_grad<GT>(a.g[i], e0, valid, g);
-        load_f32(a.m[i], e0, valid, m);
+        load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
     } else {
 #pragma unroll
         for (int j = 0; j < kVec; ++j)

@@ -75,8 +75,7 @@ __global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub
     if (valid > 0) {
         for (int i = 0; i < a.W; ++i) {
             float g[kVec], m[kVec];
-            load_grad<GT>(a.g[i], e0, valid, g);
-            load_f32(a.m[i], e0, valid, m);
+            load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
             const float inv = (NB > 1) ? a.inv[static_cast<int64_t>(i) * a.K + k] : 0.0f;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) {

@@ -42,8 +42,7 @@ __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
         float hi = 0.0f, lo = 0.0f;
         if (valid > 0) {
             float g[kVec], m[kVec];
-            load_grad<GT>(a.g[i], e0, valid, g);
-            load_f32(a.m[i], e0, valid, m);
+            load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
                 if (j < valid)
