@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "008d11353b94070f", "m1_partial": "23323d59e9d46bfb", "m1_finalize": "23323d59e9d46bfb", "reduce_apply": "f2b8c82ccf905d02"},
-    "gpt2-small-124M-w8-sign": {"compress": 10019691947, "reduce_apply": 1057647445},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040754688, "m1_finalize": 11119957, "compress": 29764585344, "reduce_apply": 4202920021},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57379323307, "reduce_apply": 3486156245},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68015596629, "m1_finalize": 44307627, "compress": 116185137408, "reduce_apply": 14105239595},
+    "fingerprints": {"compress": "593743ea8c73879a", "m1_partial": "2963c0beefaf0bc2", "m1_finalize": "2963c0beefaf0bc2", "reduce_apply": "9f0813b73ad69c2a"},
+    "gpt2-small-124M-w8-sign": {"compress": 10022135552, "reduce_apply": 1057381717},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040772053, "m1_finalize": 11121835, "compress": 29793775957, "reduce_apply": 4202640256},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391386368, "reduce_apply": 3486233771},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017147477, "m1_finalize": 44294400, "compress": 116188142037, "reduce_apply": 14104669355},
 }
 
 
