@@ -132,14 +132,18 @@ __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
 
 // ---- staged variant: the block's wire bytes arrive by bulk copy ------------
 //
-// One thread issues, per worker, one cp.async.bulk of the 256*NB bytes that
-// cover the block's 2048 elements (16-byte aligned: the block's byte offset
-// is a multiple of 256*NB and every worker's row is padded to 16 bytes) into
+// One thread issues, per worker, one cp.async.bulk of the bytes that cover
+// the block's elements (16-byte aligned: the block's byte offset is a
+// multiple of 256*NB and every worker's row is padded to 16 bytes) into
 // shared memory, completing on one mbarrier; meanwhile every thread loads its
 // theta.  The wait is bounded: if the copies have not landed after
 // kWaitLimit polls the block records an error in a.status and returns.
 
 constexpr uint32_t kWaitLimit = 1u << 20;
+// Element groups of 2048 per block (one group of 8 per thread each): the
+// block's fixed cost -- barrier set-up, copy issue, the wait -- is paid once
+// per kStagedGroups * 2048 elements.
+constexpr int kStagedGroups = 2;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
@@ -149,14 +153,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p)
 template <int NB>
 __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
 {
-    extern __shared__ __align__(128) uint8_t rows[];  // W rows of 256*NB bytes
+    extern __shared__ __align__(128) uint8_t rows[];  // W rows of kRow bytes
     __shared__ __align__(8) uint64_t bar;
-    constexpr int kRow = 256 * NB;
-    const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * (256 * kVec);
-    const int64_t e0 = blk0 + static_cast<int64_t>(threadIdx.x) * kVec;
+    constexpr int kGroupElems = 256 * kVec;          // elements per group (one per thread)
+    constexpr int kRow = kStagedGroups * 256 * NB;   // wire bytes of one worker for the block
+    const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * (kStagedGroups * kGroupElems);
     if (threadIdx.x == 0) {
         const int64_t rem = a.d - blk0;
-        const int64_t elems = rem < 256 * kVec ? rem : 256 * kVec;
+        const int64_t elems = rem < kStagedGroups * kGroupElems ? rem : kStagedGroups * kGroupElems;
         const uint32_t bytes = static_cast<uint32_t>(((elems * NB + 7) / 8 + 15) / 16 * 16);
         const uint32_t b = smem_addr(&bar);
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
@@ -169,11 +173,16 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
                          ::"r"(smem_addr(rows + i * kRow)), "l"(src + i * stride), "r"(bytes), "r"(b)
                          : "memory");
     }
-    const bool active = e0 < a.d;
-    const int valid = !active ? 0 : ((a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0));
-    float th[kVec];
-    if (active)
-        load_f32(a.theta, e0, valid, th);
+    // every group's theta is requested while the wire bytes are in flight
+    float th[kStagedGroups][kVec];
+    int valid[kStagedGroups];
+#pragma unroll
+    for (int q = 0; q < kStagedGroups; ++q) {
+        const int64_t e0 = blk0 + q * kGroupElems + static_cast<int64_t>(threadIdx.x) * kVec;
+        valid[q] = e0 >= a.d ? 0 : ((a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0));
+        if (valid[q] > 0)
+            load_f32(a.theta, e0, valid[q], th[q]);
+    }
     __syncthreads();  // the barrier is initialised before anyone polls it
     uint32_t ok = 0;
     const uint32_t b = smem_addr(&bar);
@@ -185,27 +194,30 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
             atomicExch(a.status, 1);
         return;
     }
-    if (!active)
-        return;
     using T = typename WireChunk<NB>::T;
-    int agg[kVec];
 #pragma unroll
-    for (int j = 0; j < kVec; ++j)
-        agg[j] = 0;
-    uint32_t lo = 0, hi = 0;
-    for (int i = 0; i < a.W; ++i)
-        accumulate<NB>(agg, lo, hi, reinterpret_cast<const T*>(rows + i * kRow)[threadIdx.x]);
-    if constexpr (NB == 1) {
+    for (int q = 0; q < kStagedGroups; ++q) {
+        if (valid[q] == 0)
+            continue;
+        int agg[kVec];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            agg[j] = 2 * static_cast<int>((lo >> (8 * j)) & 0xffu) - a.W;
-            agg[j + 4] = 2 * static_cast<int>((hi >> (8 * j)) & 0xffu) - a.W;
+        for (int j = 0; j < kVec; ++j)
+            agg[j] = 0;
+        uint32_t lo = 0, hi = 0;
+        for (int i = 0; i < a.W; ++i)
+            accumulate<NB>(agg, lo, hi, reinterpret_cast<const T*>(rows + i * kRow)[q * 256 + threadIdx.x]);
+        if constexpr (NB == 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                agg[j] = 2 * static_cast<int>((lo >> (8 * j)) & 0xffu) - a.W;
+                agg[j + 4] = 2 * static_cast<int>((hi >> (8 * j)) & 0xffu) - a.W;
+            }
         }
-    }
 #pragma unroll
-    for (int j = 0; j < kVec; ++j)
-        th[j] = lion_apply(th[j], direction(a, agg[j]), a.lr, a.wd);
-    store_f32(a.theta, e0, valid, th);
+        for (int j = 0; j < kVec; ++j)
+            th[q][j] = lion_apply(th[q][j], direction(a, agg[j]), a.lr, a.wd);
+        store_f32(a.theta, blk0 + q * kGroupElems + static_cast<int64_t>(threadIdx.x) * kVec, valid[q], th[q]);
+    }
 }
 
 template <int NB>
@@ -227,14 +239,14 @@ unsigned groups_grid(int64_t d)
     return static_cast<unsigned>((groups + 255) / 256);
 }
 
-// Shared memory of the staged variant: W rows of 256*NB bytes.  Above
+// Shared memory of the staged variant: W rows of kStagedGroups*256*NB bytes.  Above
 // kStagedMaxBytes the register variant runs instead.
 constexpr int kStagedMaxBytes = 64 * 1024;
 
 template <int NB>
 cudaError_t launch_nb(const StepArgs& a, unsigned grid, cudaStream_t s)
 {
-    const int smem = a.W * 256 * NB;
+    const int smem = a.W * kStagedGroups * 256 * NB;
     if (a.status != nullptr && smem <= kStagedMaxBytes) {
         if (smem > 48 * 1024) {
             const cudaError_t e =
@@ -242,7 +254,9 @@ cudaError_t launch_nb(const StepArgs& a, unsigned grid, cudaStream_t s)
             if (e != cudaSuccess)
                 return e;
         }
-        k_reduce_apply_staged<NB><<<grid, 256, smem, s>>>(a);
+        const int64_t per_block = static_cast<int64_t>(kStagedGroups) * 256 * kVec;
+        const unsigned sgrid = static_cast<unsigned>((a.d + per_block - 1) / per_block);
+        k_reduce_apply_staged<NB><<<sgrid, 256, smem, s>>>(a);
     } else {
         k_reduce_apply<NB><<<grid, 256, 0, s>>>(a);
     }
