@@ -20,6 +20,11 @@
 using lc::StepArgs;
 using lc::Tile;
 
+// Layouts the language bindings rely on.
+static_assert(sizeof(lioncub_tensor) == 24, "lioncub_tensor must stay 24 bytes");
+static_assert(sizeof(lioncub_diag) == 48, "lioncub_diag must stay 48 bytes");
+static_assert(sizeof(StepArgs) <= 4096, "kernel parameters must fit the classic 4 KB limit");
+
 struct lioncub_s {
     int device = 0;
     int64_t d = 0;

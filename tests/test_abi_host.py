@@ -117,3 +117,33 @@ def test_bench_byte_model():
     assert abs(b / W[3].d - (8 * 6 + 8 * (2 + 8 + 0.5) + 8 * 0.5 + 8)) < 1e-3
     b = bench.step_bytes(W[5])
     assert abs(b / W[5].d - (8 * 6 + 8 * (2 + 8 + 0.25) + 8 * 0.25 + 8)) < 1e-3
+
+
+def test_header_constants_match_binding(lc):
+    """Every LIONCUB_* enum value of the header equals the binding's constant."""
+    with open(os.path.join(ROOT, "include", "lioncub.h")) as f:
+        text = f.read()
+    values = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", text, re.S):
+        body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+        for name, val in re.findall(r"(LIONCUB_\w+)\s*=\s*([-0-9xA-Fa-f]+)", body):
+            values[name] = int(val, 0)
+    expect = {
+        "LIONCUB_TENSOR_SYNC_M": lc.TENSOR_SYNC_M, "LIONCUB_MODE_SIGN_MAJORITY": lc.MODE_SIGN_MAJORITY,
+        "LIONCUB_MODE_L1_INTSUM": lc.MODE_L1_INTSUM, "LIONCUB_FLAG_TIE_ALTERNATE": lc.FLAG_TIE_ALTERNATE,
+        "LIONCUB_FLAG_AVERAGE": lc.FLAG_AVERAGE, "LIONCUB_GRAD_BF16": lc.GRAD_BF16, "LIONCUB_GRAD_F32": lc.GRAD_F32,
+        "LIONCUB_OK": lc.OK, "LIONCUB_ERR_ARG": lc.ERR_ARG, "LIONCUB_ERR_ALIGN": lc.ERR_ALIGN,
+        "LIONCUB_ERR_STATE": lc.ERR_STATE, "LIONCUB_ERR_OOM": lc.ERR_OOM, "LIONCUB_ERR_CUDA": lc.ERR_CUDA,
+        "LIONCUB_MAX_WORKERS": lc.MAX_WORKERS, "LIONCUB_EXPORT_WIRE": lc.EXPORT_WIRE,
+        "LIONCUB_EXPORT_M1": lc.EXPORT_M1, "LIONCUB_EXPORT_AGG": lc.EXPORT_AGG,
+        "LIONCUB_EXPORT_STATUS": lc.EXPORT_STATUS, "LIONCUB_KERNEL_COMPRESS": lc.KERNEL_COMPRESS,
+        "LIONCUB_KERNEL_M1": lc.KERNEL_M1, "LIONCUB_KERNEL_M1_FINAL": lc.KERNEL_M1_FINAL,
+        "LIONCUB_KERNEL_REDUCE_APPLY": lc.KERNEL_REDUCE_APPLY, "LIONCUB_KERNEL_DIAGNOSE": lc.KERNEL_DIAGNOSE,
+        "LIONCUB_KERNEL_COUNT": lc.KERNEL_COUNT, "LIONCUB_NOALLOC_MAX_WORDS": lc.NOALLOC_MAX_WORDS,
+    }
+    assert set(values) == set(expect), set(values) ^ set(expect)
+    for name, v in expect.items():
+        assert values[name] == v, name
+    # struct layouts the binding assumes
+    assert ctypes.sizeof(lc.Tensor) == 24
+    assert lc.DIAG_BYTES == 48
