@@ -59,7 +59,9 @@ def build(force: bool = False) -> str:
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
            "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the oracle failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, _LIB)
     return _LIB
 

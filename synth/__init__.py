@@ -140,7 +140,9 @@ def build(force: bool = False) -> str:
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
            "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, _SRC]
-    subprocess.run(cmd, check=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the synthetic-input generator failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, _LIB)
     return _LIB
 
