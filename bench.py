@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "593743ea8c73879a", "m1_partial": "2963c0beefaf0bc2", "m1_finalize": "2963c0beefaf0bc2", "reduce_apply": "9f0813b73ad69c2a"},
-    "gpt2-small-124M-w8-sign": {"compress": 10022135552, "reduce_apply": 1057381717},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040772053, "m1_finalize": 11121835, "compress": 29793775957, "reduce_apply": 4202640256},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391386368, "reduce_apply": 3486233771},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017147477, "m1_finalize": 44294400, "compress": 116188142037, "reduce_apply": 14104669355},
+    "fingerprints": {"compress": "593743ea8c73879a", "m1_partial": "2963c0beefaf0bc2", "m1_finalize": "2963c0beefaf0bc2", "reduce_apply": "a3fd2fd33067ebba"},
+    "gpt2-small-124M-w8-sign": {"compress": 10022034304, "reduce_apply": 1058229547},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040735104, "m1_finalize": 11120597, "compress": 29794911872, "reduce_apply": 4201916075},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391548672, "reduce_apply": 3486072533},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017171200, "m1_finalize": 44296704, "compress": 116188137813, "reduce_apply": 14106390571},
 }
 
 
