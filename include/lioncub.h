@@ -178,6 +178,11 @@ LIONCUB_API int lioncub_bind_state(lioncub_t h, float* theta, float* const* m);
  * ERR_ALIGN, ERR_CUDA.  Does not synchronize.
  */
 LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream);
+/* lioncub_step only enqueues kernels (no allocation, no synchronization), so
+ * it can be captured into a CUDA graph.  The step counter advances when the
+ * step is enqueued and its parity is baked into the captured kernels (the
+ * sign of exact zeros, and the sync steps), so a loop with fixed gradient
+ * buffers captures an even and an odd step and replays them alternately. */
 
 /*
  * The same step fed from host memory: copies grads_host[0..W-1] (W host

@@ -424,3 +424,94 @@ def test_create_out_of_memory_leaks_nothing():
     # the library is still usable afterwards
     h = lc.lioncub_create(4096, 2, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
     lc.lioncub_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graphs and concurrent handles
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 4)])
+def test_step_replays_from_cuda_graphs(mode, nbits):
+    """lioncub_step only enqueues kernels, so it can be captured.  The step
+    counter advances when a step is enqueued (and its parity picks the sign
+    of exact zeros), so a loop with fixed gradient buffers captures one even
+    and one odd step and replays them alternately; the result must equal
+    plain steps bit for bit."""
+    layout = _multi_layout()
+    wl = _small(synth.layout_total(layout), 4, "bf16", mode, nbits, layout=layout, sync_interval=2)
+    ref_theta, ref_m, _ = _run_gpu(wl, 6)
+
+    dev = torch.device("cuda", 0)
+    theta = torch.empty(wl.d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(wl.d, dtype=torch.float32, device=dev) for _ in range(wl.W)]
+    grads = [torch.zeros(wl.d, dtype=torch.bfloat16, device=dev) for _ in range(wl.W)]
+    h = lc.lioncub_create(wl.d, wl.W, synth.abi_layout(layout), wl.beta1, wl.beta2, wl.lr, wl.wd, mode, nbits,
+                          lc.GRAD_BF16, 2)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        s = torch.cuda.Stream()
+        gp = [g.data_ptr() for g in grads]
+        graphs = []
+        saved = (theta.clone(), [x.clone() for x in m])
+        with torch.cuda.stream(s):
+            for _ in range(2):  # t = 0 (even) and t = 1 (odd); sync_now differs too (interval 2)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    lc.lioncub_step(h, gp, s.cuda_stream)
+                graphs.append(g)
+        torch.cuda.synchronize()
+        # capture ran nothing on the data: restore the state anyway, then replay
+        theta.copy_(saved[0])
+        for x, y in zip(m, saved[1]):
+            x.copy_(y)
+        for t in range(6):
+            for i in range(wl.W):
+                synth.fill_grad_(grads[i], wl, t, i)
+            graphs[t % 2].replay()
+        torch.cuda.synchronize()
+        assert torch.equal(theta.view(torch.int32), ref_theta.view(torch.int32))
+        for x, y in zip(m, ref_m):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    finally:
+        lc.lioncub_destroy(h)
+
+
+def test_two_handles_on_two_streams():
+    """Handles share no state: two steps running concurrently on two streams
+    give the same results as running them one after the other."""
+    wl_a = _small(300_000, 4, "bf16", 0, 1, seed=1)
+    wl_b = _small(200_000 + 45, 3, "bf16", 1, 2, seed=2)
+    ref_a = _run_gpu(wl_a, 3)
+    ref_b = _run_gpu(wl_b, 3)
+    dev = torch.device("cuda", 0)
+
+    def setup(wl):
+        theta = torch.empty(wl.d, dtype=torch.float32, device=dev)
+        synth.fill_theta_(theta, wl)
+        m = [torch.zeros(wl.d, dtype=torch.float32, device=dev) for _ in range(wl.W)]
+        grads = [[torch.empty(wl.d, dtype=torch.bfloat16, device=dev) for _ in range(wl.W)] for _ in range(3)]
+        for t in range(3):
+            for i in range(wl.W):
+                synth.fill_grad_(grads[t][i], wl, t, i)
+        h = lc.lioncub_create(wl.d, wl.W, None, wl.beta1, wl.beta2, wl.lr, wl.wd, wl.mode, wl.nbits,
+                              lc.GRAD_BF16, 0)
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        return h, theta, m, grads
+
+    ha, ta, ma, ga = setup(wl_a)
+    hb, tb, mb, gb = setup(wl_b)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        for t in range(3):
+            lc.lioncub_step(ha, [g.data_ptr() for g in ga[t]], sa.cuda_stream)
+            lc.lioncub_step(hb, [g.data_ptr() for g in gb[t]], sb.cuda_stream)
+        torch.cuda.synchronize()
+        for (theta, m), ref in (((ta, ma), ref_a), ((tb, mb), ref_b)):
+            assert torch.equal(theta.view(torch.int32), ref[0].view(torch.int32))
+            for x, y in zip(m, ref[1]):
+                assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    finally:
+        lc.lioncub_destroy(ha)
+        lc.lioncub_destroy(hb)
