@@ -21,6 +21,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "liblioncub.so")
 OBJ_DIR = os.path.join(PKG, "_build")
+# The same library with every kernel index validated in-kernel (violations set
+# a status bit instead of touching memory); used by the tests as a stand-in
+# for a memory checker.
+CHECKED_LIB = os.path.join(PKG, "liblioncub_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
@@ -46,22 +50,26 @@ def _inputs() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, bounds_check: bool = False) -> str:
+    lib = CHECKED_LIB if bounds_check else LIB
+    obj_dir = os.path.join(OBJ_DIR, "checked") if bounds_check else OBJ_DIR
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose else []
+    if bounds_check:
+        extra.append("-DLIONCUB_BOUNDS_CHECK")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *NVCC_FLAGS, *extra, f"-I{INCLUDE}", f"-I{CSRC}", "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -73,14 +81,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose="--verbose" in sys.argv))
+    print(build(force=True, verbose="--verbose" in sys.argv, bounds_check="--bounds-check" in sys.argv))

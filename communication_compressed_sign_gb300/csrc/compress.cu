@@ -91,14 +91,26 @@ __device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g,
 // worker) -- grid (tiles, W) -- so each thread handles one worker's 8
 // elements with no loop, which keeps registers low: 8 blocks of 256 threads
 // per SM (at most 32 registers), the full 2048 threads.
+// Checked builds: the element group and its wire words lie inside the
+// buffers; otherwise the group is treated as empty.
+template <int NB>
+__device__ __forceinline__ int checked_valid(const StepArgs& a, int64_t e0, int valid)
+{
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d &&
+                                        (e0 * NB) / 32 + (kVec * NB + 31) / 32 <= a.wire_stride))
+        return 0;
+    return valid;
+}
+
 template <typename GT, int NB>
 __global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int64_t tile0)
 {
-    const Tile tl = a.tiles[tile0 + blockIdx.x];
+    const int64_t tix = tile0 + blockIdx.x;
+    const Tile tl = in_bounds(a, tix < a.ntiles) ? a.tiles[tix] : Tile{0, 0, 0u};
     const int i = blockIdx.y;
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
-    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    const int valid = checked_valid<NB>(a, e0, left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left)));
     float g[kVec], m[kVec];
     if (valid > 0) {
         load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
@@ -108,8 +120,11 @@ __global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int6
             g[j] = m[j] = 0.0f;
     }
     float inv = 0.0f;
-    if constexpr (NB > 1)
-        inv = a.inv[static_cast<int64_t>(i) * a.K + (tl.meta & ~kTileSync)];
+    if constexpr (NB > 1) {
+        const uint32_t k = tl.meta & ~kTileSync;
+        if (in_bounds(a, k < static_cast<uint32_t>(a.K)))
+            inv = a.inv[static_cast<int64_t>(i) * a.K + k];
+    }
     const uint64_t bits = compress8<NB>(a, g, m, valid, inv);
     store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
     if (valid > 0)
@@ -170,11 +185,14 @@ struct Raw8<float> {
 template <typename GT, int NB>
 __global__ void __launch_bounds__(kThreads) k_compress_sync(const StepArgs a, int64_t tile0)
 {
-    const Tile tl = a.tiles[tile0 + blockIdx.x];
+    const int64_t tix = tile0 + blockIdx.x;
+    const Tile tl = in_bounds(a, tix < a.ntiles) ? a.tiles[tix] : Tile{0, 0, 0u};
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
-    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
-    const int k = static_cast<int>(tl.meta & ~kTileSync);
+    const int valid = checked_valid<NB>(a, e0, left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left)));
+    int k = static_cast<int>(tl.meta & ~kTileSync);
+    if (!in_bounds(a, k < a.K))
+        k = 0;
 
     float acc[kVec];
 #pragma unroll

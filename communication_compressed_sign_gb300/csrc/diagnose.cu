@@ -58,11 +58,15 @@ __global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub
 {
     __shared__ unsigned long long red[kThreads / 32][5];
     __shared__ float redmax[kThreads / 32];
-    const Tile tl = a.tiles[blockIdx.x];
+    const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
-    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
-    const int k = static_cast<int>(tl.meta & ~kTileSync);
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
+        valid = 0;
+    int k = static_cast<int>(tl.meta & ~kTileSync);
+    if (!in_bounds(a, k < a.K))
+        k = 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     int agg[kVec];

@@ -53,6 +53,32 @@ struct StepArgs {
     float tie_u;        // u for agg == 0: 0, or the step's zero sign
 };
 
+// Bounds-checked builds (-DLIONCUB_BOUNDS_CHECK): every global index a kernel
+// computes is validated before use; a violation sets bit 1 of the status word
+// and the access is skipped (the thread keeps taking part in shuffles and
+// barriers, so nothing traps or hangs).  Ordinary builds compile the checks
+// away.
+#ifdef LIONCUB_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+constexpr int kStatusWaitTimeout = 1;
+constexpr int kStatusOutOfBounds = 2;
+
+#ifdef __CUDACC__
+// True when an access may proceed; records a violation in checked builds.
+__device__ __forceinline__ bool in_bounds(const StepArgs& a, bool ok)
+{
+    if constexpr (kBoundsCheck) {
+        if (!ok && a.status)
+            atomicOr(a.status, kStatusOutOfBounds);
+        return ok;
+    }
+    return true;
+}
+#endif
+
 // Kernel launchers (return the launch status).
 cudaError_t launch_compress(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s);
 cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s);

@@ -32,10 +32,12 @@ __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
     // worker suffices: thread 0 has read slot (i & 1) before it reaches the
     // barrier of worker i + 1, and slot (i & 1) is rewritten only at i + 2.
     __shared__ float2 red[2][kThreads / 32];
-    const Tile tl = a.tiles[blockIdx.x];
+    const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = tl.start + tl.len - e0;
-    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
+        valid = 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     for (int i = 0; i < a.W; ++i) {
@@ -77,7 +79,9 @@ __global__ void __launch_bounds__(kFinalThreads) k_m1_finalize(const StepArgs a)
     __shared__ double red[kFinalThreads / 32];
     const int i = blockIdx.x / a.K, k = blockIdx.x % a.K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = a.tile_range[2 * k], t1 = a.tile_range[2 * k + 1];
+    int t0 = a.tile_range[2 * k], t1 = a.tile_range[2 * k + 1];
+    if (!in_bounds(a, i < a.W && 0 <= t0 && t0 <= t1 && t1 <= a.ntiles))
+        t0 = t1 = 0;
     const float2* p = a.partials + static_cast<int64_t>(i) * a.ntiles;
     double s = 0.0;
     for (int t = t0 + threadIdx.x; t < t1; t += kFinalThreads) {

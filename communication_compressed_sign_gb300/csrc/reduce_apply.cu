@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
     if (e0 >= a.d)
         return;
     const int valid = (a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0);
+    if (!in_bounds(a, (e0 * NB) / 32 + (kVec * NB + 31) / 32 <= a.wire_stride))
+        return;
     int agg[kVec];
     aggregate8<NB>(a, e0, agg);
     float th[kVec];
@@ -161,14 +163,18 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
     if (threadIdx.x == 0) {
         const int64_t rem = a.d - blk0;
         const int64_t elems = rem < kStagedGroups * kGroupElems ? rem : kStagedGroups * kGroupElems;
-        const uint32_t bytes = static_cast<uint32_t>(((elems * NB + 7) / 8 + 15) / 16 * 16);
+        uint32_t bytes = static_cast<uint32_t>(((elems * NB + 7) / 8 + 15) / 16 * 16);
+        // each worker's copy stays inside its padded row and the shared row
+        if (!in_bounds(a, elems > 0 && bytes <= static_cast<uint32_t>(kRow) &&
+                              blk0 * NB / 8 + bytes <= a.wire_stride * 4))
+            bytes = 0;
         const uint32_t b = smem_addr(&bar);
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes * a.W) : "memory");
         const uint8_t* src = reinterpret_cast<const uint8_t*>(a.wire) + blk0 * NB / 8;
         const int64_t stride = a.wire_stride * 4;
-        for (int i = 0; i < a.W; ++i)
+        for (int i = 0; bytes > 0 && i < a.W; ++i)
             asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                          ::"r"(smem_addr(rows + i * kRow)), "l"(src + i * stride), "r"(bytes), "r"(b)
                          : "memory");
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
                      : "=r"(ok) : "r"(b) : "memory");
     if (!ok) {
         if (threadIdx.x == 0)
-            atomicExch(a.status, 1);
+            atomicOr(a.status, kStatusWaitTimeout);
         return;
     }
     using T = typename WireChunk<NB>::T;
@@ -227,6 +233,8 @@ __global__ void __launch_bounds__(256) k_export_agg(const StepArgs a, int32_t* o
     if (e0 >= a.d)
         return;
     const int valid = (a.d - e0 >= kVec) ? kVec : static_cast<int>(a.d - e0);
+    if (!in_bounds(a, (e0 * NB) / 32 + (kVec * NB + 31) / 32 <= a.wire_stride))
+        return;
     int agg[kVec];
     aggregate8<NB>(a, e0, agg);
     for (int j = 0; j < valid; ++j)

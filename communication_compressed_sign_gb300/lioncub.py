@@ -16,7 +16,9 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "liblioncub.so")
+# LIONCUB_LIBRARY may name another build of the same library (the tests use
+# the bounds-checked build this way).
+LIB_PATH = os.environ.get("LIONCUB_LIBRARY") or os.path.join(_PKG, "liblioncub.so")
 
 # enums of include/lioncub.h
 TENSOR_SYNC_M = 1

@@ -227,7 +227,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
         status = torch.ones(1, dtype=torch.int32, device=dev)
         lc.lioncub_debug_export(h, lc.EXPORT_STATUS, status.data_ptr(), stream.cuda_stream)
         torch.cuda.synchronize()
-        assert int(status.item()) == 0, "a kernel reported a timed-out wait"
+        assert int(status.item()) == 0, "a kernel reported a timed-out wait or an out-of-bounds index"
         return rep
     finally:
         lc.lioncub_destroy(h)
@@ -290,6 +290,10 @@ def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_
         torch.cuda.synchronize()
         assert lc.lioncub_get_step(h) == t and torch.equal(theta, theta_before)  # nothing updated
         gpu = lc.decode_diag(out.cpu().numpy().tobytes(), K)
+        status = torch.ones(1, dtype=torch.int32, device=dev)
+        lc.lioncub_debug_export(h, lc.EXPORT_STATUS, status.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, "a kernel reported a timed-out wait or an out-of-bounds index"
         res = []
         for k, (name, off, n, fl) in enumerate(wl.layout):
             if name not in tensor_names:

@@ -359,7 +359,10 @@ def test_guard_bands_untouched(mode, nbits, d, sync):
             lc.lioncub_step(h, [x[1].data_ptr() for x in gs], torch.cuda.current_stream().cuda_stream)
         out = torch.empty(len(layout) * lc.DIAG_BYTES, dtype=torch.uint8, device=theta.device)
         lc.lioncub_diagnose(h, [x[1].data_ptr() for x in gs], out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        status = torch.ones(1, dtype=torch.int32, device=theta.device)
+        lc.lioncub_debug_export(h, lc.EXPORT_STATUS, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
         torch.cuda.synchronize()
+        assert int(status.item()) == 0
         for buf, inner, g in [(tb, theta, gt)] + ms + gs:
             raw = buf.view(torch.uint8)
             eb = buf.element_size()
