@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "593743ea8c73879a", "m1_partial": "2963c0beefaf0bc2", "m1_finalize": "2963c0beefaf0bc2", "reduce_apply": "a3fd2fd33067ebba"},
-    "gpt2-small-124M-w8-sign": {"compress": 10022034304, "reduce_apply": 1058229547},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040735104, "m1_finalize": 11120597, "compress": 29794911872, "reduce_apply": 4201916075},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391548672, "reduce_apply": 3486072533},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017171200, "m1_finalize": 44296704, "compress": 116188137813, "reduce_apply": 14106390571},
+    "fingerprints": {"compress": "32e3f9cc7d8d7b56", "m1_partial": "c67a4190b47245fe", "m1_finalize": "c67a4190b47245fe", "reduce_apply": "17889972b545f85b"},
+    "gpt2-small-124M-w8-sign": {"compress": 10022261248, "reduce_apply": 1057687595},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041379499, "m1_finalize": 11120683, "compress": 29793469611, "reduce_apply": 4201454592},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391224363, "reduce_apply": 3485693696},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016273493, "m1_finalize": 44311723, "compress": 116188786475, "reduce_apply": 14106163200},
 }
 
 
