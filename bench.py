@@ -320,19 +320,24 @@ def run_gpu(args, wl: synth.Workload):
             lc.lioncub_step(h, gptrs[s % nsets], sp)
             ev[s][1].record(stream)
         torch.cuda.synchronize(dev)
-        total_ms = sum(a.elapsed_time(b) for a, b in ev)
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        total_ms = sum(step_ms)
     else:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        # back-to-back steps; an event between consecutive steps gives each
+        # step's time without adding work to the stream
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev[0].record(stream)
         for s in range(args.steps):
             lc.lioncub_step(h, gptrs[s % nsets], sp)
-        e1.record(stream)
+            ev[s + 1].record(stream)
         torch.cuda.synchronize(dev)
-        total_ms = e0.elapsed_time(e1)
+        step_ms = [ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps)]
+        total_ms = ev[0].elapsed_time(ev[-1])
     barrier(dev)
     clk = clocks.stop()
     ms_local = total_ms / args.steps
     ms = reduce_max(ms_local, dev)
+    ms_median = reduce_max(float(statistics.median(step_ms)), dev)
 
     kb = kernel_bytes(wl)
     per_kernel = {}
@@ -360,6 +365,15 @@ def run_gpu(args, wl: synth.Workload):
     # end to end: host gradients in, host theta out, through lioncub_step_host
     e2e = None if args.no_e2e else run_e2e(args, wl, h, dev, stream)
 
+    # the device status word (bounded waits that gave up, guard bands around
+    # the library's scratch), read after all timing: a run that tripped it is
+    # not a valid measurement
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    lc.lioncub_debug_export(h, lc.EXPORT_STATUS, status.data_ptr(), stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status word is {int(status.item())} after the timed steps")
+
     lc.lioncub_destroy(h)
     del grads, m, theta, flush_buf
     torch.cuda.empty_cache()
@@ -372,6 +386,7 @@ def run_gpu(args, wl: synth.Workload):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms,
+        "ms_per_step_median": ms_median,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,

@@ -15,6 +15,7 @@
 #include <string>
 #include <vector>
 
+#include "guard.h"
 #include "internal.h"
 
 using lc::StepArgs;
@@ -24,6 +25,9 @@ using lc::Tile;
 static_assert(sizeof(lioncub_tensor) == 24, "lioncub_tensor must stay 24 bytes");
 static_assert(sizeof(lioncub_diag) == 48, "lioncub_diag must stay 48 bytes");
 static_assert(sizeof(StepArgs) <= 4096, "kernel parameters must fit the classic 4 KB limit");
+static_assert(lc::kStatusWaitTimeout == LIONCUB_STATUS_WAIT_TIMEOUT &&
+                  lc::kStatusOutOfBounds == LIONCUB_STATUS_OUT_OF_BOUNDS && lc::kStatusGuard == LIONCUB_STATUS_GUARD,
+              "status bits are part of the ABI");
 
 struct lioncub_s {
     int device = 0;
@@ -47,7 +51,10 @@ struct lioncub_s {
     int64_t wire_words = 0;   // per worker, dense
     int64_t wire_stride = 0;  // per worker, padded to 4 words
 
-    // device scratch owned by the library
+    // device scratch owned by the library: every allocation lioncub_create
+    // made (allocs), and the guard bands around the buffers kernels write
+    std::vector<void*> allocs;
+    lc::GuardList guards{};
     uint32_t* wire = nullptr;
     Tile* tiles = nullptr;
     int32_t* tile_range = nullptr;
@@ -66,6 +73,12 @@ struct lioncub_s {
     cudaEvent_t ev_used[2] = {nullptr, nullptr};
     bool used_recorded[2] = {false, false};
     int64_t host_calls = 0;
+
+    // fault injection (environment, read at create): the fail_alloc_at-th
+    // device allocation and the fail_launch_at-th step launch of the handle
+    // report an error instead of running (0 = off)
+    int64_t fail_alloc_at = 0, alloc_count = 0;
+    int64_t fail_launch_at = 0, launch_count = 0;
 
     // profiling
     int prof_steps_left = 0;   // steps still to record
@@ -107,9 +120,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_scratch(lioncub_t h)
 {
-    void* ptrs[] = {h->wire, h->tiles, h->tile_range, h->numel, h->partials, h->m1, h->inv, h->status,
-                    h->staging[0], h->staging[1]};
-    for (void* p : ptrs)
+    for (void* p : h->allocs)
+        cudaFree(p);
+    h->allocs.clear();
+    h->guards.n = 0;
+    for (void* p : h->staging)
         if (p)
             cudaFree(p);
     h->wire = nullptr;
@@ -145,13 +160,72 @@ void drop_profile(lioncub_t h)
     h->prof_this_call = false;
 }
 
-template <typename T>
-cudaError_t dev_alloc(T** p, size_t count)
+// A positive integer from the environment, else 0.
+int64_t env_index(const char* name)
+{
+    const char* v = std::getenv(name);
+    if (!v || !*v)
+        return 0;
+    char* end = nullptr;
+    const long long x = std::strtoll(v, &end, 10);
+    return (*end == '\0' && x > 0) ? static_cast<int64_t>(x) : 0;
+}
+
+// Every device allocation of a handle goes through here, so that fault
+// injection can fail any one of them.
+cudaError_t raw_alloc(lioncub_t h, void** p, size_t bytes)
 {
     *p = nullptr;
-    if (count == 0)
-        count = 1;
-    return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+    if (++h->alloc_count == h->fail_alloc_at)
+        return cudaErrorMemoryAllocation;
+    return cudaMalloc(p, bytes);
+}
+
+// count elements of T for the handle's lifetime (freed by free_scratch).
+template <typename T>
+cudaError_t dev_alloc(lioncub_t h, T** p, size_t count)
+{
+    void* base = nullptr;
+    *p = nullptr;
+    const cudaError_t e = raw_alloc(h, &base, (count ? count : 1) * sizeof(T));
+    if (e != cudaSuccess)
+        return e;
+    h->allocs.push_back(base);
+    *p = static_cast<T*>(base);
+    return cudaSuccess;
+}
+
+// The same for a buffer that kernels write, between two guard bands of
+// lc::kGuardBytes.  The buffer keeps cudaMalloc's 256-byte alignment.
+template <typename T>
+cudaError_t guarded_alloc(lioncub_t h, T** p, size_t count)
+{
+    static_assert(lc::kGuardBytes % 256 == 0 && sizeof(T) % 4 == 0, "guards keep alignment");
+    const size_t inner = (count ? count : 1) * sizeof(T);
+    char* base = nullptr;
+    *p = nullptr;
+    if (h->guards.n + 2 > lc::kMaxGuardBands)
+        return cudaErrorInvalidValue;
+    cudaError_t e = dev_alloc(h, &base, lc::kGuardBytes + inner + lc::kGuardBytes);
+    if (e != cudaSuccess)
+        return e;
+    char* back = base + lc::kGuardBytes + inner;
+    e = cudaMemset(base, static_cast<int>(lc::kGuardByte), lc::kGuardBytes);
+    if (e == cudaSuccess)
+        e = cudaMemset(back, static_cast<int>(lc::kGuardByte), lc::kGuardBytes);
+    if (e != cudaSuccess)
+        return e;
+    h->guards.band[h->guards.n++] = reinterpret_cast<const uint32_t*>(base);
+    h->guards.band[h->guards.n++] = reinterpret_cast<const uint32_t*>(back);
+    *p = reinterpret_cast<T*>(base + lc::kGuardBytes);
+    return cudaSuccess;
+}
+
+// Fault injection: the error the handle's next step launch reports instead
+// of launching, or cudaSuccess.
+cudaError_t injected_launch_fault(lioncub_t h)
+{
+    return (++h->launch_count == h->fail_launch_at) ? cudaErrorLaunchOutOfResources : cudaSuccess;
 }
 
 StepArgs make_args(lioncub_t h, const void* const* grads)
@@ -363,18 +437,24 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
     h->wire_words = (d * h->nbits + 31) / 32;
     h->wire_stride = (h->wire_words + 3) / 4 * 4;
 
+    h->fail_alloc_at = env_index("LIONCUB_FAIL_ALLOC");
+    h->fail_launch_at = env_index("LIONCUB_FAIL_LAUNCH");
     cudaError_t e = cudaGetDevice(&h->device);
-    if (e == cudaSuccess) e = dev_alloc(&h->wire, static_cast<size_t>(W) * h->wire_stride + 4);
-    if (e == cudaSuccess) e = dev_alloc(&h->tiles, tiles.size());
-    if (e == cudaSuccess) e = dev_alloc(&h->tile_range, first.size());
-    if (e == cudaSuccess) e = dev_alloc(&h->numel, numel.size());
-    if (e == cudaSuccess) e = dev_alloc(&h->status, 1);
+    if (e == cudaSuccess) e = guarded_alloc(h, &h->wire, static_cast<size_t>(W) * h->wire_stride + 4);
+    if (e == cudaSuccess) e = dev_alloc(h, &h->tiles, tiles.size());
+    if (e == cudaSuccess) e = dev_alloc(h, &h->tile_range, first.size());
+    if (e == cudaSuccess) e = dev_alloc(h, &h->numel, numel.size());
+    if (e == cudaSuccess) e = dev_alloc(h, &h->status, 1);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
     if (e == cudaSuccess && h->mode == LIONCUB_MODE_L1_INTSUM) {
-        e = dev_alloc(&h->partials, static_cast<size_t>(W) * h->ntiles);
-        if (e == cudaSuccess) e = dev_alloc(&h->m1, static_cast<size_t>(W) * h->K);
-        if (e == cudaSuccess) e = dev_alloc(&h->inv, static_cast<size_t>(W) * h->K);
+        e = guarded_alloc(h, &h->partials, static_cast<size_t>(W) * h->ntiles);
+        if (e == cudaSuccess) e = guarded_alloc(h, &h->m1, static_cast<size_t>(W) * h->K);
+        if (e == cudaSuccess) e = guarded_alloc(h, &h->inv, static_cast<size_t>(W) * h->K);
     }
+    // Fault injection: one byte of the guard band after the wire buffer is
+    // overwritten, as an overrunning kernel would.
+    if (e == cudaSuccess && env_index("LIONCUB_POISON_GUARD") > 0)
+        e = cudaMemset(const_cast<uint32_t*>(h->guards.band[1]), 0, 1);
     if (e == cudaSuccess && !tiles.empty())
         e = cudaMemcpy(h->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
@@ -383,6 +463,11 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
         e = cudaMemcpy(h->numel, numel.data(), numel.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
         e = cudaMemset(h->wire, 0, (static_cast<size_t>(W) * h->wire_stride + 4) * sizeof(uint32_t));
+    // The set-up copies and fills above are ordered on the legacy default
+    // stream and may still be in flight; wait for them, so that steps on any
+    // stream (non-blocking ones included) see the finished tables.
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(nullptr);
     if (e != cudaSuccess) {
         const int code = (e == cudaErrorMemoryAllocation) ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA;
         cudaGetLastError();  // clear a non-sticky allocation error
@@ -441,23 +526,31 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
     int slot;
     if (l1) {
         slot = prof_begin(h, LIONCUB_KERNEL_M1, s);
-        e = lc::launch_m1_partial(a, h->grad_dtype, s);
+        e = injected_launch_fault(h);
+        if (e == cudaSuccess)
+            e = lc::launch_m1_partial(a, h->grad_dtype, s);
         prof_end(h, slot, s);
         if (e != cudaSuccess)
             return cuda_fail(h, e, "m1_partial launch");
         slot = prof_begin(h, LIONCUB_KERNEL_M1_FINAL, s);
-        e = lc::launch_m1_finalize(a, s);
+        e = injected_launch_fault(h);
+        if (e == cudaSuccess)
+            e = lc::launch_m1_finalize(a, s);
         prof_end(h, slot, s);
         if (e != cudaSuccess)
             return cuda_fail(h, e, "m1_finalize launch");
     }
     slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
-    e = lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s);
+    e = injected_launch_fault(h);
+    if (e == cudaSuccess)
+        e = lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s);
     prof_end(h, slot, s);
     if (e != cudaSuccess)
         return cuda_fail(h, e, "compress launch");
     slot = prof_begin(h, LIONCUB_KERNEL_REDUCE_APPLY, s);
-    e = lc::launch_reduce_apply(a, l1 ? 1 : 0, s);
+    e = injected_launch_fault(h);
+    if (e == cudaSuccess)
+        e = lc::launch_reduce_apply(a, l1 ? 1 : 0, s);
     prof_end(h, slot, s);
     if (e != cudaSuccess)
         return cuda_fail(h, e, "reduce_apply launch");
@@ -497,7 +590,7 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
             return cuda_fail(h, e, "host-step set-up");
         const size_t bytes = gstride * h->W + 256;
         for (int b = 0; b < 2; ++b) {
-            e = cudaMalloc(&h->staging[b], bytes);
+            e = raw_alloc(h, &h->staging[b], bytes);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 h->staging[b] = nullptr;
@@ -601,7 +694,9 @@ int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t 
                             cudaMemcpyDeviceToDevice, s);
         break;
     case LIONCUB_EXPORT_STATUS:
-        e = cudaMemcpyAsync(dst_dev, h->status, sizeof(int), cudaMemcpyDeviceToDevice, s);
+        e = lc::launch_guard_check(h->guards, h->status, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dst_dev, h->status, sizeof(int), cudaMemcpyDeviceToDevice, s);
         break;
     case LIONCUB_EXPORT_AGG: {
         const StepArgs a = make_args(h, nullptr);

@@ -31,6 +31,7 @@ GRAD_F32 = 1
 OK, ERR_ARG, ERR_ALIGN, ERR_STATE, ERR_OOM, ERR_CUDA = 0, -1, -2, -3, -4, -5
 MAX_WORKERS = 128
 EXPORT_WIRE, EXPORT_M1, EXPORT_AGG, EXPORT_STATUS = 0, 1, 2, 3
+STATUS_WAIT_TIMEOUT, STATUS_OUT_OF_BOUNDS, STATUS_GUARD = 1, 2, 4
 KERNEL_COMPRESS, KERNEL_M1, KERNEL_M1_FINAL, KERNEL_REDUCE_APPLY, KERNEL_DIAGNOSE, KERNEL_COUNT = 0, 1, 2, 3, 4, 5
 KERNEL_NAMES = {KERNEL_COMPRESS: "compress", KERNEL_M1: "m1_partial",
                 KERNEL_M1_FINAL: "m1_finalize", KERNEL_REDUCE_APPLY: "reduce_apply",

@@ -53,6 +53,17 @@
  * surface as LIONCUB_ERR_CUDA at a later call or at the caller's stream
  * synchronization.  No call synchronizes the device except the ones marked
  * "synchronizes".
+ *
+ * Fault injection for tests (environment variables, read by lioncub_create
+ * for the handle it creates; unset, they cost nothing):
+ *   LIONCUB_FAIL_ALLOC=k   the handle's k-th device allocation (lioncub_create's
+ *                          first, then lioncub_step_host's staging) fails as
+ *                          out of memory;
+ *   LIONCUB_FAIL_LAUNCH=k  the handle's k-th step kernel launch reports
+ *                          cudaErrorLaunchOutOfResources without launching;
+ *   LIONCUB_POISON_GUARD=1 one byte of the guard band after the wire buffer is
+ *                          overwritten at creation, so the next status export
+ *                          reports LIONCUB_STATUS_GUARD.
  */
 #ifndef LIONCUB_H
 #define LIONCUB_H
@@ -113,8 +124,17 @@ enum {
     LIONCUB_EXPORT_WIRE = 0, /* W x lioncub_wire_words() uint32: last step's packed words/codes */
     LIONCUB_EXPORT_M1 = 1,   /* W x K float: last step's M1 (L1 mode)               */
     LIONCUB_EXPORT_AGG = 2,  /* d int32: the aggregate of the last step's wire words */
-    LIONCUB_EXPORT_STATUS = 3 /* 1 int32: 0, or 1 once a kernel's bounded wait for its own
-                                 bulk copies gave up (the step's theta is then invalid) */
+    LIONCUB_EXPORT_STATUS = 3 /* 1 int32 of LIONCUB_STATUS_* bits, 0 when all is well */
+};
+
+/* Bits of the device status word (sticky until lioncub_destroy). */
+enum {
+    LIONCUB_STATUS_WAIT_TIMEOUT = 1,  /* a kernel's bounded wait for its own bulk copies gave
+                                         up; that step's theta is invalid                */
+    LIONCUB_STATUS_OUT_OF_BOUNDS = 2, /* bounds-checked builds only: a kernel computed an
+                                         index outside its buffer and skipped the access  */
+    LIONCUB_STATUS_GUARD = 4          /* a guard band around the library's scratch buffers
+                                         was overwritten (checked at each status export) */
 };
 
 /* Per-tensor diagnostics of a step (lioncub_diagnose), 48 bytes. */
@@ -152,6 +172,8 @@ enum {
  * lioncub_destroy; the caller's layout array is copied.  Errors: ERR_ARG,
  * ERR_ALIGN, ERR_OOM, ERR_CUDA (*out is set to NULL).  Uses the current
  * CUDA device, which must stay current for every later call on the handle.
+ * Synchronizes the legacy default stream once, at the end, so the tables it
+ * uploaded are in place before a step on any stream reads them.
  */
 LIONCUB_API int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layout, int K,
                    float beta1, float beta2, float lr, float wd, int mode, int nbits,
@@ -174,8 +196,12 @@ LIONCUB_API int lioncub_bind_state(lioncub_t h, float* theta, float* const* m);
  * gradients of the handle's dtype, 16-byte aligned; the host array is read
  * during the call only, the device buffers must stay unchanged until the
  * step has run.  theta and m are updated in place; the step counter advances
- * only if every launch was enqueued.  Errors: ERR_STATE (unbound), ERR_ARG,
- * ERR_ALIGN, ERR_CUDA.  Does not synchronize.
+ * only if every launch was enqueued.  Launch order: (L1 mode: M1 pass, M1
+ * combine,) compress (writes the wire and m), reduce_apply (writes theta).
+ * If the compress launch or one before it fails, theta and m are unchanged
+ * and the step can be retried; if reduce_apply fails, m has already moved,
+ * so restore the state from a checkpoint.  Errors: ERR_STATE (unbound),
+ * ERR_ARG, ERR_ALIGN, ERR_CUDA.  Does not synchronize.
  */
 LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream);
 /* lioncub_step only enqueues kernels (no allocation, no synchronization), so
@@ -218,8 +244,10 @@ LIONCUB_API int64_t lioncub_wire_words(lioncub_t h);
  * Fig. 8 captions (packed 0/1 signs, p-bit integer containers); M1 of Eq. (1).
  * Copy diagnostic data of the last step into dst_dev (device memory the
  * caller owns; sizes in the LIONCUB_EXPORT_* comments) on `stream`.  For
- * LIONCUB_EXPORT_AGG a kernel recomputes the aggregate from the wire words.
- * For tests; never part of a timed step.
+ * LIONCUB_EXPORT_AGG a kernel recomputes the aggregate from the wire words;
+ * for LIONCUB_EXPORT_STATUS a kernel first checks the guard bands (256
+ * bytes before and after each of the wire, M1-partial, M1 and 1/M1
+ * buffers).  For tests; never part of a timed step.
  */
 LIONCUB_API int lioncub_debug_export(lioncub_t h, int what, void* dst_dev, lioncub_stream_t stream);
 

@@ -140,6 +140,8 @@ def test_header_constants_match_binding(lc):
         "LIONCUB_KERNEL_M1": lc.KERNEL_M1, "LIONCUB_KERNEL_M1_FINAL": lc.KERNEL_M1_FINAL,
         "LIONCUB_KERNEL_REDUCE_APPLY": lc.KERNEL_REDUCE_APPLY, "LIONCUB_KERNEL_DIAGNOSE": lc.KERNEL_DIAGNOSE,
         "LIONCUB_KERNEL_COUNT": lc.KERNEL_COUNT, "LIONCUB_NOALLOC_MAX_WORDS": lc.NOALLOC_MAX_WORDS,
+        "LIONCUB_STATUS_WAIT_TIMEOUT": lc.STATUS_WAIT_TIMEOUT, "LIONCUB_STATUS_OUT_OF_BOUNDS": lc.STATUS_OUT_OF_BOUNDS,
+        "LIONCUB_STATUS_GUARD": lc.STATUS_GUARD,
     }
     assert set(values) == set(expect), set(values) ^ set(expect)
     for name, v in expect.items():
