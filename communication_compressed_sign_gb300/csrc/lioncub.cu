@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "guard.h"
+#include "host_io.h"
 #include "internal.h"
 
 using lc::StepArgs;
@@ -117,6 +118,21 @@ int cuda_fail(lioncub_t h, cudaError_t e, const char* what)
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The device address of a page-locked host buffer mapped into the device's
+// address space (16-byte aligned), else nullptr: pageable memory, or memory
+// the device cannot address, which a copy engine then moves.
+float* mapped_host_view(float* p)
+{
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();  // not a CUDA pointer: clear the non-sticky error
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer || !aligned16(attr.devicePointer))
+        return nullptr;
+    return static_cast<float*>(attr.devicePointer);
+}
 
 void free_scratch(lioncub_t h)
 {
@@ -631,7 +647,12 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
     e = cudaEventRecord(h->ev_used[b], s);
     if (e == cudaSuccess) {
         h->used_recorded[b] = true;
-        if (h->d)
+        // theta download: SM stores into a mapped page-locked buffer (the
+        // copy engine stays with the next upload), else a copy
+        float* mapped = h->d ? mapped_host_view(theta_host_out) : nullptr;
+        if (mapped)
+            e = lc::launch_store_host(h->theta, mapped, h->d, s);
+        else if (h->d)
             e = cudaMemcpyAsync(theta_host_out, h->theta, static_cast<size_t>(h->d) * sizeof(float),
                                 cudaMemcpyDeviceToHost, s);
     }

@@ -220,7 +220,10 @@ LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stre
  * The uploads run on an internal non-blocking stream into one of two staging
  * buffers (allocated on the first call, kept until destroy; one if memory is
  * short), so the next call's upload overlaps this call's kernels and theta
- * download; `stream` waits for the upload before the step's kernels.
+ * download; `stream` waits for the upload before the step's kernels.  When
+ * theta_host_out is page-locked memory mapped into the device's address
+ * space (e.g. from cudaHostAlloc) and 16-byte aligned, SM threads store theta
+ * into it, leaving the copy engine to the uploads; otherwise it is copied.
  * Errors as lioncub_step, plus ERR_OOM for the staging.
  */
 LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
