@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "32e3f9cc7d8d7b56", "m1_partial": "c67a4190b47245fe", "m1_finalize": "c67a4190b47245fe", "reduce_apply": "17889972b545f85b"},
-    "gpt2-small-124M-w8-sign": {"compress": 10022261248, "reduce_apply": 1057687595},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041379499, "m1_finalize": 11120683, "compress": 29793469611, "reduce_apply": 4201454592},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57391224363, "reduce_apply": 3485693696},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016273493, "m1_finalize": 44311723, "compress": 116188786475, "reduce_apply": 14106163200},
+    "fingerprints": {"compress": "f3da110000003175", "m1_partial": "dfe9c533416cc79d", "m1_finalize": "dfe9c533416cc79d", "reduce_apply": "52a4c728de4eda3e"},
+    "gpt2-small-124M-w8-sign": {"compress": 10022268245, "reduce_apply": 1057867051},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041155328, "m1_finalize": 11120299, "compress": 29793626069, "reduce_apply": 4201697109},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57390691883, "reduce_apply": 3485788331},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017360853, "m1_finalize": 44303701, "compress": 116189161685, "reduce_apply": 14106443179},
 }
 
 

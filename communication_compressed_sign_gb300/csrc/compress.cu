@@ -87,10 +87,6 @@ __device__ __forceinline__ uint64_t compress8(const StepArgs& a, const float* g,
     return bits;
 }
 
-// Tiles whose momentum is not synchronized this step: one block per (tile,
-// worker) -- grid (tiles, W) -- so each thread handles one worker's 8
-// elements with no loop, which keeps registers low: 8 blocks of 256 threads
-// per SM (at most 32 registers), the full 2048 threads.
 // Checked builds: the element group and its wire words lie inside the
 // buffers; otherwise the group is treated as empty.
 template <int NB>
@@ -102,6 +98,10 @@ __device__ __forceinline__ int checked_valid(const StepArgs& a, int64_t e0, int 
     return valid;
 }
 
+// Tiles whose momentum is not synchronized this step: one block per (tile,
+// worker) -- grid (tiles, W) -- so each thread handles one worker's 8
+// elements with no loop, which keeps registers low: 8 blocks of 256 threads
+// per SM (at most 32 registers), the full 2048 threads.
 template <typename GT, int NB>
 __global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int64_t tile0)
 {

@@ -8,9 +8,10 @@
 // hi/lo pair carrying ~48 significant bits; TwoSum per element), reduced over
 // the warp with shuffles and over the 8 warps in a fixed order, and stores
 // the (hi, lo) pair.  Looping over the workers inside the block amortizes the
-// block's start-up and its serial final merge over W tiles' worth of data.  GB300 runs fp64 at a small fraction of its fp32 rate, so a
-// per-element fp64 add would cap this pass below memory speed; the pair keeps
-// the per-tile sum accurate to far below one fp32 ulp of the mean.
+// block's start-up and its serial final merge over W tiles' worth of data.
+// GB300 runs fp64 at a small fraction of its fp32 rate, so a per-element fp64
+// add would cap this pass below memory speed; the pair keeps the per-tile sum
+// accurate to far below one fp32 ulp of the mean.
 //
 // Pass 2 (k_m1_finalize): one block per (worker, tensor) sums its tiles'
 // pairs in fp64 -- thread t takes tiles t, t+256, ... in order, then a fixed

@@ -139,7 +139,9 @@ __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
 // multiple of 256*NB and every worker's row is padded to 16 bytes) into
 // shared memory, completing on one mbarrier; meanwhile every thread loads its
 // theta.  The wait is bounded: if the copies have not landed after
-// kWaitLimit polls the block records an error in a.status and returns.
+// kWaitLimit polls the block records an error in a.status, waits once more
+// (bounded the same way) for its copies to land, so that none is still
+// writing to the block's shared memory when it is released, and returns.
 
 constexpr uint32_t kWaitLimit = 1u << 20;
 // Element groups of 2048 per block (one group of 8 per thread each): the
@@ -150,6 +152,17 @@ constexpr int kStagedGroups = 2;
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Polls the mbarrier at shared address b until phase 0 completes, at most
+// kWaitLimit times; true when it completed.
+__device__ __forceinline__ bool wait_phase0(uint32_t b)
+{
+    uint32_t ok = 0;
+    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it)
+        asm volatile("{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0;\n selp.u32 %0, 1, 0, P;\n}"
+                     : "=r"(ok) : "r"(b) : "memory");
+    return ok != 0;
 }
 
 template <int NB>
@@ -190,14 +203,11 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
             load_f32(a.theta, e0, valid[q], th[q]);
     }
     __syncthreads();  // the barrier is initialised before anyone polls it
-    uint32_t ok = 0;
     const uint32_t b = smem_addr(&bar);
-    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it)
-        asm volatile("{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0;\n selp.u32 %0, 1, 0, P;\n}"
-                     : "=r"(ok) : "r"(b) : "memory");
-    if (!ok) {
+    if (!wait_phase0(b)) {
         if (threadIdx.x == 0)
             atomicOr(a.status, kStatusWaitTimeout);
+        wait_phase0(b);  // drain this block's copies before leaving
         return;
     }
     using T = typename WireChunk<NB>::T;
