@@ -662,6 +662,29 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
     return LIONCUB_OK;
 }
 
+int lioncub_host_alloc(void** out, size_t bytes)
+{
+    if (!out)
+        return LIONCUB_ERR_ARG;
+    *out = nullptr;
+    if (bytes == 0)
+        return LIONCUB_OK;
+    const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocPortable | cudaHostAllocMapped);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return fail(nullptr, e == cudaErrorMemoryAllocation ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA,
+                    "page-locked allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    }
+    return LIONCUB_OK;
+}
+
+void lioncub_host_free(void* p)
+{
+    if (p)
+        cudaFreeHost(p);
+}
+
 int lioncub_set_lr(lioncub_t h, float lr)
 {
     if (!h)

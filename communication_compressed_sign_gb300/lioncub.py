@@ -45,7 +45,7 @@ EXPORTED = (
     "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step", "lioncub_wire_words",
     "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read",
     "lioncub_last_error", "lioncub_strerror", "lioncub_destroy", "lioncub_sign_step_noalloc",
-    "lioncub_diagnose",
+    "lioncub_diagnose", "lioncub_host_alloc", "lioncub_host_free",
 )
 NOALLOC_MAX_WORDS = 4194304
 
@@ -98,6 +98,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.lioncub_sign_step_noalloc.restype = i32
         L.lioncub_diagnose.argtypes = [vp, vp, vp, vp]
         L.lioncub_diagnose.restype = i32
+        L.lioncub_host_alloc.argtypes = [ctypes.POINTER(vp), ctypes.c_size_t]
+        L.lioncub_host_alloc.restype = i32
+        L.lioncub_host_free.argtypes = [vp]
+        L.lioncub_host_free.restype = None
         for name in ("lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
                      "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step",
                      "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read"):
@@ -144,6 +148,49 @@ def lioncub_step(h: int, grad_ptrs, stream: int = 0) -> None:
 def lioncub_step_host(h: int, grad_host_ptrs, theta_host_out_ptr: int, stream: int = 0) -> None:
     _check(load().lioncub_step_host(h, ctypes.cast(_ptrs(grad_host_ptrs), ctypes.c_void_p),
                                     theta_host_out_ptr, stream or None), h)
+
+
+def lioncub_host_alloc(nbytes: int) -> int:
+    """Page-locked, device-mapped host memory for lioncub_step_host; 0 for 0 bytes."""
+    p = ctypes.c_void_p()
+    _check(load().lioncub_host_alloc(ctypes.byref(p), nbytes), None)
+    return p.value or 0
+
+
+def lioncub_host_free(ptr: int) -> None:
+    load().lioncub_host_free(ptr or None)
+
+
+class HostBuffer:
+    """A lioncub_host_alloc block viewed as a CPU torch tensor of `numel`
+    elements of `dtype`; the memory is released by close() (or when the
+    object is collected).  Keep the object alive while the tensor is used."""
+
+    def __init__(self, numel: int, dtype):
+        import torch
+        itemsize = torch.empty(0, dtype=dtype).element_size()
+        self.nbytes = int(numel) * itemsize
+        self.ptr = lioncub_host_alloc(self.nbytes)
+        if self.nbytes:
+            raw = (ctypes.c_char * self.nbytes).from_address(self.ptr)
+            self.tensor = torch.frombuffer(raw, dtype=dtype, count=int(numel))
+        else:
+            self.tensor = torch.empty(0, dtype=dtype)
+
+    def data_ptr(self) -> int:
+        return self.ptr
+
+    def close(self) -> None:
+        if self.ptr:
+            self.tensor = None
+            lioncub_host_free(self.ptr)
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def lioncub_set_lr(h: int, lr: float) -> None:

@@ -68,6 +68,7 @@
 #ifndef LIONCUB_H
 #define LIONCUB_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 /* Exported entry points keep default visibility even when the library is
@@ -228,6 +229,18 @@ LIONCUB_API int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stre
  */
 LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_host_out,
                       lioncub_stream_t stream);
+
+/*
+ * Page-locked host memory for lioncub_step_host's buffers: `bytes` bytes,
+ * mapped into every device's address space, allocated directly by the CUDA
+ * runtime (no caching allocator in between), so that uploads from it and
+ * theta stores into it run at the host link's full rate.  *out is set to
+ * NULL when bytes == 0.  The memory stays valid until lioncub_host_free.
+ * Errors: ERR_ARG (out NULL), ERR_OOM (message via lioncub_last_error(NULL)).
+ * lioncub_host_free releases it (NULL is a no-op); it synchronizes the device.
+ */
+LIONCUB_API int lioncub_host_alloc(void** out, size_t bytes);
+LIONCUB_API void lioncub_host_free(void* p);
 
 /* Learning rate of later steps (textbook Lion's lr). */
 LIONCUB_API int lioncub_set_lr(lioncub_t h, float lr);

@@ -83,13 +83,14 @@ class ParityReport:
 
 
 def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, strict: bool = True,
-               use_host_step: bool = False, host_pinned: bool = True, grad_hook=None):
+               use_host_step: bool = False, host_mem: str = "library", grad_hook=None):
     """Run `steps` steps of workload `wl` on the GPU and on the oracle (over
     `pieces`); return a ParityReport.  With strict=True, assert the bounds.
     grad_hook(t, i, tensor), if given, edits worker i's step-t gradients on
     the GPU after they are generated (both sides see the edited bits).
-    use_host_step runs lioncub_step_host from page-locked host buffers
-    (host_pinned) or pageable ones, and checks its theta output too."""
+    use_host_step runs lioncub_step_host from host buffers of kind host_mem
+    ("library": lioncub_host_alloc, "torch": torch's pinned allocator,
+    "pageable") and checks its theta output too."""
     import torch
 
     dev = torch.device("cuda", 0)
@@ -146,9 +147,14 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
         pinned = None
         theta_host = None
         if use_host_step:
+            keep = []
+
             def host_buf(dtype):
+                if host_mem == "library":
+                    keep.append(lc.HostBuffer(d, dtype))
+                    return keep[-1].tensor
                 x = torch.empty(d, dtype=dtype)
-                return x.pin_memory() if host_pinned else x
+                return x.pin_memory() if host_mem == "torch" else x
             pinned = [host_buf(gdt) for _ in range(W)]
             theta_host = host_buf(torch.float32)
 

@@ -32,11 +32,22 @@ def _declared():
 
 def test_header_symbols_exported(lc):
     declared = _declared()
-    assert len(declared) == 16
+    assert len(declared) == 18
     lib = ctypes.CDLL(lc.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name
     assert sorted(lc.EXPORTED) == declared
+
+
+def test_host_alloc_argument_checks(lc):
+    """The page-locked allocator validates its arguments before touching
+    CUDA: a NULL out pointer is ERR_ARG, zero bytes gives NULL and OK."""
+    L = lc.load()
+    assert L.lioncub_host_alloc(None, 64) == lc.ERR_ARG
+    p = ctypes.c_void_p(1234)
+    assert L.lioncub_host_alloc(ctypes.byref(p), 0) == lc.OK
+    assert not p.value
+    L.lioncub_host_free(None)  # a no-op
 
 
 def test_create_validation_codes(lc):

@@ -152,15 +152,16 @@ def test_exact_zero_update_vectors():
         parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 5, grad_hook=_zero_pattern)
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_host_buffer_entry_point(pinned):
-    """lioncub_step_host from page-locked buffers (theta stored into the
-    mapped output by SM threads) and from pageable ones (copies); a vector
-    length that is not a multiple of 4 covers the download's tail."""
+@pytest.mark.parametrize("host_mem", ["library", "torch", "pageable"])
+def test_host_buffer_entry_point(host_mem):
+    """lioncub_step_host from page-locked buffers (lioncub_host_alloc or
+    torch's pinned allocator: theta stored into the mapped output by SM
+    threads) and from pageable ones (copies); a vector length that is not a
+    multiple of 4 covers the download's tail."""
     wl = _small(70000, 4, "bf16", 0, 1)
-    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True, host_pinned=pinned)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True, host_mem=host_mem)
     wl = _small(70001, 3, "f32", 1, 4)
-    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True, host_pinned=pinned)
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 3, use_host_step=True, host_mem=host_mem)
 
 
 # ---------------------------------------------------------------------------
