@@ -70,7 +70,9 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
+            # LIONCUB_ORACLE_LIB: a separately built copy of this source (the
+            # mutation test loads deliberately broken copies through it)
+            path = os.environ.get("LIONCUB_ORACLE_LIB") or build()
             L = ctypes.CDLL(path)
             f32, i64, i32, u32 = ctypes.c_float, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
             vp = ctypes.c_void_p

@@ -283,6 +283,44 @@ def test_single_worker_is_textbook_lion(oracle_lib):
         assert np.array_equal(m[0].view(np.uint32), m_ref.view(np.uint32)), t
 
 
+def test_bf16_gradients_equal_their_fp32_values(oracle_lib):
+    """A bf16 number is the upper half of the fp32 bit pattern of the same
+    value (bfloat16 format: 1 sign, 8 exponent, 7 fraction bits).  So
+    (1) the bf16 patterns 0x3F80, 0xC020, 0x3E20 and 0x0000 are 1.0, -2.5,
+    0.15625 and 0.0, which a single step from m = 0 exposes as
+    m' = RN(omega2 * g); and (2) gradients whose fp32 patterns have a zero low
+    half give the same step -- wire words, theta, m, in both modes -- whether
+    passed as bf16 patterns or as fp32."""
+    b2 = 0.99
+    om2 = np.float32(1.0) - np.float32(b2)
+    g16 = np.array([0x3F80, 0xC020, 0x3E20, 0x0000], dtype=np.uint16)
+    values = np.array([1.0, -2.5, 0.15625, 0.0], dtype=np.float32)
+    m = [np.zeros(4, np.float32)]
+    oracle.step(d=4, W=1, layout=None, beta1=0.9, beta2=b2, lr=1e-4, wd=0.1, mode=oracle.MODE_SIGN,
+                nbits=1, flags=0, sync_interval=0, t=0, grads=[g16], theta=np.zeros(4, np.float32), m=m)
+    assert np.array_equal(m[0], om2 * values)
+
+    rng = np.random.default_rng(5)
+    d, W = 3000, 3
+    g32 = [((rng.standard_t(3, d) * 1e-3).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000))
+           .view(np.float32) for _ in range(W)]
+    g16 = [(x.view(np.uint32) >> 16).astype(np.uint16) for x in g32]
+    theta0 = rng.uniform(-0.05, 0.05, d).astype(np.float32)
+    layout = [(0, 1024, 0), (1024, d - 1024, 0)]
+    for mode, nbits in ((oracle.MODE_SIGN, 1), (oracle.MODE_L1, 4)):
+        runs = []
+        for grads in (g32, g16):
+            theta, m = theta0.copy(), [np.zeros(d, np.float32) for _ in range(W)]
+            outs = [oracle.step(d=d, W=W, layout=layout, beta1=0.9, beta2=0.99, lr=1e-4, wd=0.1, mode=mode,
+                                nbits=nbits, flags=0, sync_interval=0, t=t, grads=grads, theta=theta, m=m)
+                    for t in range(3)]
+            runs.append((theta, m, outs[-1].wire))
+        (ta, ma, wa), (tb, mb, wb) = runs
+        assert np.array_equal(ta.view(np.uint32), tb.view(np.uint32))
+        for x, y in zip(ma + wa, mb + wb):
+            assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
 def test_omega(oracle_lib):
     assert oracle.omega(0.9) == np.float32(1.0) - np.float32(0.9)
     assert oracle.omega(0.5) == 0.5
@@ -443,6 +481,17 @@ def test_diagnose_hand_cases(oracle_lib):
     r = oracle.diagnose(d=1, W=2, layout=None, beta1=0.0, mode=oracle.MODE_SIGN, nbits=1,
                         flags=oracle.FLAG_TIE_ALTERNATE, t=0, grads=g2, m=m2)[0]
     assert (r["match"], r["dropped"], r["ties"]) == (1, 0, 1)
+
+
+def test_diagnose_max_std_is_a_maximum_per_tensor(oracle_lib):
+    """Two workers, m0 = 0 and m1 = (1, 4, 2 | 6, 0): the per-element std is
+    |m1| / 2, so the per-tensor maxima are 2 (second element, not the first)
+    and 3."""
+    m = [np.zeros(5, np.float32), np.array([1, 4, 2, 6, 0], np.float32)]
+    g = [np.zeros(5, np.float32), np.zeros(5, np.float32)]
+    rs = oracle.diagnose(d=5, W=2, layout=[(0, 3, 0), (3, 2, 0)], beta1=0.9, mode=oracle.MODE_SIGN, nbits=1,
+                         flags=0, t=0, grads=g, m=m)
+    assert [r["max_std_m"] for r in rs] == [2.0, 3.0]
 
 
 def test_diagnose_l1_uses_q1_codes(oracle_lib):
