@@ -78,6 +78,24 @@ def test_workload5_xl_l1_n2():
     print(rep)
 
 
+@pytest.mark.parametrize("key,names,steps", [
+    (3, ("wte",), 2),
+    (4, ("wte",), 3),
+    (5, ("wte", "head", "h0.mlp.c_fc.w"), 2),
+])
+def test_largest_tensors_whole(key, names, steps):
+    """The largest tensors of the 350M and 1.3B workloads, whole, at full
+    size and in the benchmark's launch configuration: every element's wire
+    field, aggregate, theta and momentum against the oracle (51.5M to 222.6M
+    parameters, 8 or 16 workers; the momentum-synchronized embedding of the
+    16-worker workload included)."""
+    wl = WL[key]
+    pieces = _names(wl, *names)
+    assert sum(p.n for p in pieces) >= 51_000_000
+    rep = parity.run_parity(wl, pieces, steps)
+    print(rep)
+
+
 # ---------------------------------------------------------------------------
 # small cases
 # ---------------------------------------------------------------------------
