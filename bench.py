@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "f3da110000003175", "m1_partial": "dfe9c533416cc79d", "m1_finalize": "dfe9c533416cc79d", "reduce_apply": "52a4c728de4eda3e"},
-    "gpt2-small-124M-w8-sign": {"compress": 10022268245, "reduce_apply": 1057867051},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041155328, "m1_finalize": 11120299, "compress": 29793626069, "reduce_apply": 4201697109},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57390691883, "reduce_apply": 3485788331},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68017360853, "m1_finalize": 44303701, "compress": 116189161685, "reduce_apply": 14106443179},
+    "fingerprints": {"compress": "8835b9eefe04219d", "m1_partial": "e35bf0c20c799a38", "m1_finalize": "e35bf0c20c799a38", "reduce_apply": "43565cbf8557d20a"},
+    "gpt2-small-124M-w8-sign": {"compress": 10021307605, "reduce_apply": 1058014805},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041244800, "m1_finalize": 11120768, "compress": 29791031680, "reduce_apply": 4201665963},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57375409451, "reduce_apply": 3485816491},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016206763, "m1_finalize": 44297515, "compress": 116179067477, "reduce_apply": 14106725547},
 }
 
 

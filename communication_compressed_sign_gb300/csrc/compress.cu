@@ -37,7 +37,10 @@ __device__ __forceinline__ int q1_code(float c, float inv, int qmax)
 }
 
 // Write this thread's 8*NB wire bits (in `bits`, low bits first) of the tile
-// element group starting at e0 into the worker's wire words.
+// element group starting at e0 into the worker's wire words.  Streaming
+// (evict-first) stores: at these sizes the wire does not stay in L2 until the
+// reduce reads it anyway, and keeping it out of L2's way measured 2.7-3.1 %
+// faster for the L1 codes (0.6 % for 1-bit signs) than cache-global stores.
 template <int NB>
 __device__ __forceinline__ void store_wire(uint32_t* wire_i, int64_t e0, int valid, uint64_t bits)
 {
@@ -48,18 +51,18 @@ __device__ __forceinline__ void store_wire(uint32_t* wire_i, int64_t e0, int val
                            (__shfl_down_sync(0xffffffffu, b, 2) << 16) |
                            (__shfl_down_sync(0xffffffffu, b, 3) << 24);
         if ((lane & 3) == 0 && valid > 0)
-            __stcg(wire_i + (e0 >> 5), w);
+            __stcs(wire_i + (e0 >> 5), w);
     } else if constexpr (NB == 2) {
         const uint32_t h = static_cast<uint32_t>(bits);
         const uint32_t w = h | (__shfl_down_sync(0xffffffffu, h, 1) << 16);
         if ((lane & 1) == 0 && valid > 0)
-            __stcg(wire_i + (e0 >> 4), w);
+            __stcs(wire_i + (e0 >> 4), w);
     } else if constexpr (NB == 4) {
         if (valid > 0)
-            __stcg(wire_i + (e0 >> 3), static_cast<uint32_t>(bits));
+            __stcs(wire_i + (e0 >> 3), static_cast<uint32_t>(bits));
     } else {
         if (valid > 0)
-            __stcg(reinterpret_cast<uint2*>(wire_i + (e0 >> 2)),
+            __stcs(reinterpret_cast<uint2*>(wire_i + (e0 >> 2)),
                    make_uint2(static_cast<uint32_t>(bits), static_cast<uint32_t>(bits >> 32)));
     }
 }

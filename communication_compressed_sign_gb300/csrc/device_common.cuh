@@ -16,7 +16,7 @@ namespace lc {
 
 // --- gradient loads: 8 consecutive elements -> 8 floats ---------------------
 // Gradients and momenta are read once per step, so loads use the streaming
-// (evict-first) cache hint and leave L2 to the small wire buffer.
+// (evict-first) cache hint.
 
 __device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
