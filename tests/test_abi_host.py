@@ -2,12 +2,14 @@
 
 No GPU is touched: the library is loaded, every symbol that include/lioncub.h
 declares must be exported, and argument validation (which runs before any
-CUDA call) must return the documented codes.
+CUDA call) must return the documented codes.  (A layout that passes
+validation goes on to the device set-up, which fails without a GPU.)
 """
 import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import synth
@@ -80,6 +82,68 @@ def test_create_validation_codes(lc):
     assert create(64, 2, [(0, 32, 0), (0, 32, 0)]) == lc.ERR_ARG       # overlaps
     assert create(64, 2, [(0, 64, 4)]) == lc.ERR_ARG                   # unknown tensor flag
     assert h.value is None
+
+
+def _layout_verdict(d, layout):
+    """The documented layout contract, written independently of the library:
+    tensors tile [0, d) in order, every offset a multiple of 32 (checked first
+    for each tensor), non-negative sizes, known flags only."""
+    nxt = 0
+    for (off, n, fl) in layout:
+        if off % 32:
+            return "align"
+        if off != nxt or n < 0:
+            return "arg"
+        if fl & ~1:
+            return "arg"
+        nxt += n
+    return "ok" if nxt == d else "arg"
+
+
+def test_create_layout_fuzz(lc):
+    """Random layouts (ragged, overlapping, gapped, misaligned, negative,
+    unknown flags) get the error the contract predicts; valid ones reach
+    the device set-up (ERR_CUDA without a GPU, a handle with one)."""
+    L = lc.load()
+    rng = np.random.default_rng(2024)
+    sizes = [0, 1, 31, 32, 33, 64, 100, 2048, 4096 + 7]
+    counts = {"ok": 0, "arg": 0, "align": 0}
+    for _ in range(400):
+        K = int(rng.integers(1, 7))
+        layout, off = [], 0
+        for k in range(K):
+            n = int(rng.choice(sizes))
+            if k < K - 1 and rng.random() < 0.7:
+                n = (n + 31) // 32 * 32  # inner tensors usually keep the next offset aligned
+            o = off
+            r = rng.random()
+            if r < 0.05:
+                o += 32            # gap
+            elif r < 0.10:
+                o -= 32            # overlap
+            elif r < 0.15:
+                o += 1             # misaligned
+            if rng.random() < 0.03:
+                n = -n - 1         # negative size
+            fl = int(rng.choice([0, 0, 0, 1, 2]))
+            layout.append((o, n, fl))
+            off = o + max(n, 0)
+        d = sum(max(n, 0) for (_, n, _) in layout) + (int(rng.integers(-2, 3)) if rng.random() < 0.1 else 0)
+        d = max(d, 0)
+        want = _layout_verdict(d, layout)
+        counts[want] += 1
+        arr = (lc.Tensor * K)(*[lc.Tensor(*t) for t in layout])
+        h = ctypes.c_void_p()
+        rc = L.lioncub_create(ctypes.byref(h), d, 2, ctypes.cast(arr, ctypes.c_void_p), K, 0.9, 0.99, 1e-4,
+                              0.1, 0, 1, 0, 0)
+        if want == "ok":
+            assert rc in (lc.OK, lc.ERR_CUDA, lc.ERR_OOM), (layout, d, rc)
+            if rc == lc.OK:
+                L.lioncub_destroy(h)
+        else:
+            assert rc == (lc.ERR_ALIGN if want == "align" else lc.ERR_ARG), (layout, d, rc, want)
+            assert h.value is None
+    assert min(counts.values()) >= 20, counts
 
 
 def test_null_handle_paths(lc):

@@ -8,6 +8,8 @@ the host-buffer entry point, determinism, checkpoint/resume and the error
 paths.  Sign mode must be bit-exact; L1 mode within the tolerances stated in
 tests/parity.py.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -63,8 +65,11 @@ def test_workload3_gpt2_medium_l1_n4():
     print(rep)
 
 
-def test_workload4_gpt2_medium_w16_sync():
-    wl = WL[4]
+@pytest.mark.parametrize("interval,beta2", [(1, 0.99), (10, 0.95)])
+def test_workload4_gpt2_medium_w16_sync(interval, beta2):
+    """As configured (sync every step), and with the pages' periodic setting:
+    beta2 = 0.95 and the embedding's momentum synchronized every 10 steps."""
+    wl = dataclasses.replace(WL[4], sync_interval=interval, beta2=beta2)
     pieces = sorted(parity.chunk_pieces(wl.layout, "wte", 16, 2048, seed=4)
                     + _names(wl, "wpe", "h3.attn.c_proj.w", "ln_f.b"), key=lambda p: p.src)
     assert any(p.flags for p in pieces)
