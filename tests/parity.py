@@ -196,7 +196,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
 
             # wire words / codes
             dst, gsel = 0, 0
-            for p, (_, nw) in zip(pieces, wranges):
+            for k_sub, (p, (_, nw)) in enumerate(zip(pieces, wranges)):
                 ow0 = dst * bits // 32
                 for i in range(W):
                     gw = wire_h[i, gsel:gsel + nw]
@@ -211,7 +211,6 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
                             rep.code_offby1 += int((dd == 1).sum())
                             rep.code_worse += int((dd > 1).sum())
                 if l1 and p.tensor >= 0:
-                    k_sub = pieces.index(p)
                     g_m1 = m1[:, p.tensor].cpu().numpy()
                     o_m1 = out.m1[:, k_sub]
                     rel = np.abs(g_m1.astype(np.float64) - o_m1) / np.maximum(np.abs(o_m1), 1e-30)

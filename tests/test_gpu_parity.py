@@ -146,6 +146,23 @@ def test_multi_tensor_sync(mode, nbits, interval):
     parity.run_parity(wl, pieces, 7)
 
 
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 8)])
+def test_many_small_tensors(mode, nbits):
+    """2,000 tensors of 32 to 4,128 elements (every tile boundary case: one
+    partial tile, exactly one tile, several tiles plus a ragged one), a
+    ragged last tensor, a tenth of them momentum-synchronized every second
+    step: the per-tensor tile table, the (worker, tensor) M1 combine and
+    the split between plain and synchronized tiles at scale."""
+    rng = np.random.default_rng(77 + nbits)
+    sizes = [int(x) * 32 for x in rng.integers(1, 130, 1999)] + [45]
+    layout, off = [], 0
+    for k, n in enumerate(sizes):
+        layout.append((f"t{k}", off, n, synth.SYNC_M if rng.random() < 0.1 else 0))
+        off += n
+    wl = _small(off, 5, "bf16", mode, nbits, layout=layout, sync_interval=2, seed=nbits)
+    parity.run_parity(wl, parity.tensor_pieces(layout, {n for (n, _, _, _) in layout}), 4)
+
+
 @pytest.mark.parametrize("flags", [lc.FLAG_TIE_ALTERNATE, lc.FLAG_AVERAGE])
 @pytest.mark.parametrize("W", [2, 4, 9])
 def test_tie_and_average_rules(flags, W):
