@@ -236,7 +236,8 @@ LIONCUB_API int lioncub_step_host(lioncub_t h, const void* const* grads_host, fl
  * runtime (no caching allocator in between), so that uploads from it and
  * theta stores into it run at the host link's full rate.  *out is set to
  * NULL when bytes == 0.  The memory stays valid until lioncub_host_free.
- * Errors: ERR_ARG (out NULL), ERR_OOM (message via lioncub_last_error(NULL)).
+ * Errors: ERR_ARG (out NULL), ERR_OOM, ERR_CUDA (messages via
+ * lioncub_last_error(NULL)).
  * lioncub_host_free releases it (NULL is a no-op); it synchronizes the device.
  */
 LIONCUB_API int lioncub_host_alloc(void** out, size_t bytes);
