@@ -192,6 +192,63 @@ def test_exact_zero_update_vectors():
         parity.run_parity(wl, parity.tensor_pieces(wl.layout, {"flat"}), 5, grad_hook=_zero_pattern)
 
 
+@pytest.mark.parametrize("mode,nbits,interval", [(0, 1, 0), (1, 4, 3)])
+def test_host_steps_pipelined_back_to_back(mode, nbits, interval):
+    """Eight lioncub_step_host calls issued back to back with no host
+    synchronization, each from its own set of page-locked gradient buffers:
+    uploads run ahead into the two staging buffers while earlier steps
+    compute, so any missing ordering between an upload and the step that
+    last read its staging buffer would change the result.  theta (device and
+    host copy) and every momentum must equal eight device-buffer steps on
+    the same gradients, bit for bit."""
+    dev = torch.device("cuda", 0)
+    layout = [("a", 0, 3 << 20, synth.SYNC_M if interval else 0), ("b", 3 << 20, (1 << 20) + 77, 0)]
+    wl = _small(synth.layout_total(layout), 4, "bf16", mode, nbits, layout=layout, sync_interval=interval)
+    K = 8
+    grads = [[torch.empty(wl.d, dtype=torch.bfloat16, device=dev) for _ in range(wl.W)] for _ in range(K)]
+    for t in range(K):
+        for i in range(wl.W):
+            synth.fill_grad_(grads[t][i], wl, t, i)
+    host = [[lc.HostBuffer(wl.d, torch.bfloat16) for _ in range(wl.W)] for _ in range(K)]
+    for t in range(K):
+        for i in range(wl.W):
+            host[t][i].tensor.copy_(grads[t][i])
+    theta_out = lc.HostBuffer(wl.d, torch.float32)
+
+    def run(use_host):
+        theta = torch.empty(wl.d, dtype=torch.float32, device=dev)
+        synth.fill_theta_(theta, wl)
+        m = [torch.zeros(wl.d, dtype=torch.float32, device=dev) for _ in range(wl.W)]
+        h = lc.lioncub_create(wl.d, wl.W, synth.abi_layout(layout), wl.beta1, wl.beta2, wl.lr, wl.wd, mode, nbits,
+                              lc.GRAD_BF16, interval)
+        try:
+            lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+            torch.cuda.synchronize()
+            s = torch.cuda.current_stream().cuda_stream
+            for t in range(K):
+                if use_host:
+                    lc.lioncub_step_host(h, [x.data_ptr() for x in host[t]], theta_out.data_ptr(), s)
+                else:
+                    lc.lioncub_step(h, [x.data_ptr() for x in grads[t]], s)
+            torch.cuda.synchronize()
+        finally:
+            lc.lioncub_destroy(h)
+        return theta, m
+
+    try:
+        th_a, m_a = run(False)
+        th_b, m_b = run(True)
+        assert torch.equal(th_a.view(torch.int32), th_b.view(torch.int32))
+        assert torch.equal(theta_out.tensor.view(torch.int32), th_a.cpu().view(torch.int32))
+        for x, y in zip(m_a, m_b):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    finally:
+        for row in host:
+            for x in row:
+                x.close()
+        theta_out.close()
+
+
 @pytest.mark.parametrize("host_mem", ["library", "torch", "pageable"])
 def test_host_buffer_entry_point(host_mem):
     """lioncub_step_host from page-locked buffers (lioncub_host_alloc or
