@@ -32,18 +32,23 @@ class LionCubOptimizer:
         self._keep = None
 
     def bind(self, theta, m):
+        import torch
+        if len(m) != self.W:
+            raise ValueError(f"expected {self.W} momentum tensors")
         for x in (theta, *m):
-            if not (x.is_cuda and x.is_contiguous()) or x.dtype.itemsize != 4 or x.numel() != self.d:
+            if not (x.is_cuda and x.is_contiguous()) or x.dtype != torch.float32 or x.numel() != self.d:
                 raise ValueError("theta and m must be contiguous float32 CUDA tensors of d elements")
         lioncub.lioncub_bind_state(self.h, theta.data_ptr(), [x.data_ptr() for x in m])
         self._keep = (theta, list(m))
 
     def step(self, grads, stream=None):
+        import torch
         if len(grads) != self.W:
             raise ValueError(f"expected {self.W} gradient tensors")
+        want = torch.bfloat16 if self.grad_dtype == GRAD_BF16 else torch.float32
         for g in grads:
-            if not (g.is_cuda and g.is_contiguous()) or g.numel() != self.d:
-                raise ValueError("gradients must be contiguous CUDA tensors of d elements")
+            if not (g.is_cuda and g.is_contiguous()) or g.dtype != want or g.numel() != self.d:
+                raise ValueError(f"gradients must be contiguous {want} CUDA tensors of d elements")
         s = stream.cuda_stream if stream is not None else _current_stream()
         lioncub.lioncub_step(self.h, [g.data_ptr() for g in grads], s)
 

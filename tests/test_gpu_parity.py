@@ -511,6 +511,10 @@ def test_optimizer_wrapper_matches_c_abi():
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     with pytest.raises(ValueError):
         opt.step(grads[:-1])
+    with pytest.raises(ValueError):
+        opt.step([g.float() for g in grads])  # the handle takes bf16 gradients
+    with pytest.raises(ValueError):
+        opt.bind(theta, m[:-1])
     opt.close()
 
 
