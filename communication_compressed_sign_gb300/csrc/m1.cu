@@ -13,11 +13,14 @@
 // add would cap this pass below memory speed; the pair keeps the per-tile sum
 // accurate to far below one fp32 ulp of the mean.
 //
-// Pass 2 (k_m1_finalize): one block per (worker, tensor) sums its tiles'
-// pairs in fp64 -- thread t takes tiles t, t+256, ... in order, then a fixed
-// xor-butterfly per warp and the warps in order -- divides by numel in fp64,
-// rounds once to fp32, and stores M1 and the scale inv = RN(qmax / M1) (0
-// when M1 == 0).
+// Pass 2 (k_m1_finalize): one block per (worker, tensor).  Thread t merges
+// the pairs of tiles t, t+256, ... in order into its own compensated fp32
+// pair, converts it to fp64 once, and the block combines the threads in fp64
+// -- a fixed xor-butterfly per warp, then the warps in order -- divides by
+// numel in fp64, rounds once to fp32, and stores M1 and the scale
+// inv = RN(qmax / M1) (0 when M1 == 0).  Converting and adding every tile's
+// pair in fp64 instead kept the narrow fp64 pipe of the SMs holding the
+// largest tensors 71 % busy and made those blocks the long pole.
 //
 // Both passes have fixed tilings and fixed reduction orders, so M1 is
 // bit-for-bit deterministic from run to run.
@@ -70,9 +73,9 @@ __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
     }
 }
 
-// One block per (worker, tensor): thread t sums tiles t, t + 256, ... of the
-// tensor in fp64, then a fixed xor-butterfly per warp and the 8 warp sums in
-// order.
+// One block per (worker, tensor): thread t merges tiles t, t + 256, ... of
+// the tensor (compensated fp32), then fp64: a fixed xor-butterfly per warp
+// and the 8 warp sums in order.
 constexpr int kFinalThreads = 256;
 
 __global__ void __launch_bounds__(kFinalThreads) k_m1_finalize(const StepArgs a)
@@ -84,11 +87,12 @@ __global__ void __launch_bounds__(kFinalThreads) k_m1_finalize(const StepArgs a)
     if (!in_bounds(a, i < a.W && 0 <= t0 && t0 <= t1 && t1 <= a.ntiles))
         t0 = t1 = 0;
     const float2* p = a.partials + static_cast<int64_t>(i) * a.ntiles;
-    double s = 0.0;
-    for (int t = t0 + threadIdx.x; t < t1; t += kFinalThreads) {
+    float hi = 0.0f, lo = 0.0f;
+    for (int64_t t = t0 + static_cast<int64_t>(threadIdx.x); t < t1; t += kFinalThreads) {
         const float2 v = p[t];
-        s = __dadd_rn(s, __dadd_rn(static_cast<double>(v.x), static_cast<double>(v.y)));
+        cacc_merge(hi, lo, v.x, v.y);
     }
+    double s = __dadd_rn(static_cast<double>(hi), static_cast<double>(lo));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
