@@ -54,11 +54,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "8835b9eefe04219d", "m1_partial": "6257ba576300c4ea", "m1_finalize": "6257ba576300c4ea", "reduce_apply": "43565cbf8557d20a"},
-    "gpt2-small-124M-w8-sign": {"compress": 10021226197, "reduce_apply": 1057940437},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040817152, "m1_finalize": 11112832, "compress": 29790167808, "reduce_apply": 4201714645},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57374300800, "reduce_apply": 3485763712},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016553899, "m1_finalize": 44287275, "compress": 116178187179, "reduce_apply": 14106464128},
+    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "aaff01b04ec58e36", "m1_finalize": "aaff01b04ec58e36", "reduce_apply": "32648b6ee9a13fce"},
+    "gpt2-small-124M-w8-sign": {"compress": 10021211563, "reduce_apply": 1057834283},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040765056, "m1_finalize": 11113557, "compress": 29790780757, "reduce_apply": 4201562667},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57374447531, "reduce_apply": 3485934891},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016781781, "m1_finalize": 44287147, "compress": 116177724117, "reduce_apply": 14106499456},
 }
 
 

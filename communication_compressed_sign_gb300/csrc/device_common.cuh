@@ -117,6 +117,57 @@ __device__ __forceinline__ void load_gm(const void* g, const float* m, int64_t e
     }
 }
 
+// Raw 16-byte vectors of 8 gradients (bf16: one uint4; fp32: two float4)
+// and 8 momenta of a full group, kept packed while they wait in registers
+// (software pipelines load the next worker's Raw8 before computing this one).
+template <typename GT>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 g;
+    float4 m0, m1;
+    // kKeepM: the momenta are read again soon, so they take the default
+    // cache policy instead of the streaming one
+    template <bool kKeepM = false>
+    __device__ __forceinline__ void load(const void* gb, const float* mb, int64_t e0)
+    {
+        g = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(gb) + e0));
+        const float4* q = reinterpret_cast<const float4*>(mb + e0);
+        m0 = kKeepM ? q[0] : __ldcs(q);
+        m1 = kKeepM ? q[1] : __ldcs(q + 1);
+    }
+    __device__ __forceinline__ void unpack(float* gv, float* mv) const
+    {
+        gv[0] = bf16_bits_lo(g.x); gv[1] = bf16_bits_hi(g.x);
+        gv[2] = bf16_bits_lo(g.y); gv[3] = bf16_bits_hi(g.y);
+        gv[4] = bf16_bits_lo(g.z); gv[5] = bf16_bits_hi(g.z);
+        gv[6] = bf16_bits_lo(g.w); gv[7] = bf16_bits_hi(g.w);
+        mv[0] = m0.x; mv[1] = m0.y; mv[2] = m0.z; mv[3] = m0.w;
+        mv[4] = m1.x; mv[5] = m1.y; mv[6] = m1.z; mv[7] = m1.w;
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 g0, g1, m0, m1;
+    template <bool kKeepM = false>
+    __device__ __forceinline__ void load(const void* gb, const float* mb, int64_t e0)
+    {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(gb) + e0);
+        g0 = __ldcs(p);
+        g1 = __ldcs(p + 1);
+        const float4* q = reinterpret_cast<const float4*>(mb + e0);
+        m0 = kKeepM ? q[0] : __ldcs(q);
+        m1 = kKeepM ? q[1] : __ldcs(q + 1);
+    }
+    __device__ __forceinline__ void unpack(float* gv, float* mv) const
+    {
+        gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w;
+        gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+        mv[0] = m0.x; mv[1] = m0.y; mv[2] = m0.z; mv[3] = m0.w;
+        mv[4] = m1.x; mv[5] = m1.y; mv[6] = m1.z; mv[7] = m1.w;
+    }
+};
+
 __device__ __forceinline__ void store_f32(float* base, int64_t e0, int valid, const float* x)
 {
     if (valid == kVec) {

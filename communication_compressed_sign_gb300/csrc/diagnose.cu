@@ -17,7 +17,9 @@
 // std = sqrt(var), all in fp32 with one rounding per operation.
 //
 // One block per tile; each thread takes 8 elements and loops over the
-// workers (a second loop re-reads the momenta for the variance).  Per-tensor
+// workers, software-pipelined on full groups (a second loop re-reads the
+// momenta for the variance; the first loop reads them with the default cache
+// policy so that the second finds them in L2).  Per-tensor
 // totals are combined with integer atomics (exact, order-free) and the
 // maximum with an integer atomicMax on the non-negative float's bits.
 #include "device_common.cuh"
@@ -76,18 +78,35 @@ __global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub
         agg[j] = 0;
         s[j] = ms[j] = 0.0f;
     }
-    if (valid > 0) {
+    // per worker: c, its wire value, and the running sums of c and m
+    auto accumulate = [&](int i, const float* g, const float* m) {
+        const float inv = (NB > 1) ? a.inv[static_cast<int64_t>(i) * a.K + k] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
+            agg[j] += wire_value<NB>(c, inv, a.qmax, a.zero_bit);
+            s[j] = (i == 0) ? c : __fadd_rn(s[j], c);
+            ms[j] = (i == 0) ? m[j] : __fadd_rn(ms[j], m[j]);
+        }
+    };
+    if (valid == kVec) {
+        // full groups: worker i+1's loads are issued before worker i is used
+        // the momenta stay cached for the variance pass below
+        Raw8<GT> cur, nxt;
+        cur.template load<true>(a.g[0], a.m[0], e0);
+        for (int i = 0; i < a.W; ++i) {
+            if (i + 1 < a.W)
+                nxt.template load<true>(a.g[i + 1], a.m[i + 1], e0);
+            float g[kVec], m[kVec];
+            cur.unpack(g, m);
+            accumulate(i, g, m);
+            cur = nxt;
+        }
+    } else if (valid > 0) {
         for (int i = 0; i < a.W; ++i) {
             float g[kVec], m[kVec];
             load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
-            const float inv = (NB > 1) ? a.inv[static_cast<int64_t>(i) * a.K + k] : 0.0f;
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
-                agg[j] += wire_value<NB>(c, inv, a.qmax, a.zero_bit);
-                s[j] = (i == 0) ? c : __fadd_rn(s[j], c);
-                ms[j] = (i == 0) ? m[j] : __fadd_rn(ms[j], m[j]);
-            }
+            accumulate(i, g, m);
         }
     }
     const float fw = static_cast<float>(a.W);
