@@ -54,11 +54,13 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "aaff01b04ec58e36", "m1_finalize": "aaff01b04ec58e36", "reduce_apply": "32648b6ee9a13fce"},
-    "gpt2-small-124M-w8-sign": {"compress": 10021211563, "reduce_apply": 1057834283},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17040765056, "m1_finalize": 11113557, "compress": 29790780757, "reduce_apply": 4201562667},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57374447531, "reduce_apply": 3485934891},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016781781, "m1_finalize": 44287147, "compress": 116177724117, "reduce_apply": 14106499456},
+    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "aaff01b04ec58e36", "m1_finalize": "aaff01b04ec58e36", "reduce_apply": "b33f05b058ff3387"},
+    "gpt2-small-124M-w8-sign": {"compress": 10021207851, "reduce_apply": 1057754880},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041085867, "m1_finalize": 11115349, "compress": 29790421717, "reduce_apply": 4201522261},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57373891200, "reduce_apply": 3485637888},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016455467, "m1_finalize": 44290091, "compress": 116178687360, "reduce_apply": 14107258667},
+    "vit-b16-86M-w8-dlion-avg": {"compress": 6953046187, "reduce_apply": 717670016},
+    "deit-tiny-5.5M-w8-l1n4-embed-head-sync": {"m1_partial": 266411221, "m1_finalize": 195157, "compress": 400234539, "reduce_apply": 44369664},
 }
 
 
@@ -101,6 +103,20 @@ def kernel_bytes(wl: synth.Workload) -> dict:
 
 def step_bytes(wl: synth.Workload) -> int:
     return sum(kernel_bytes(wl).values())
+
+
+def mode_label(wl: synth.Workload) -> str:
+    if wl.mode == 1:
+        return f"L1 n={wl.nbits} + int sum"
+    return "sign + D-Lion average" if wl.flags & 0x200 else "sign+majority"
+
+
+def sync_label(wl: synth.Workload) -> str:
+    flagged = [name for (name, _, _, fl) in wl.layout if fl]
+    if not wl.sync_interval or not flagged:
+        return "none"
+    every = "every step" if wl.sync_interval == 1 else f"every {wl.sync_interval} steps"
+    return f"{', '.join(flagged)} {every}"
 
 
 # ---------------------------------------------------------------------------
@@ -233,7 +249,7 @@ def time_oracle_steps(wl: synth.Workload, target_elems: int, steps: int, warmup:
     for t in range(warmup + steps):
         t0 = time.perf_counter()
         oracle.step(d=dsub, W=wl.W, layout=sub, beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr, wd=wl.wd,
-                    mode=wl.mode, nbits=wl.nbits, flags=0, sync_interval=wl.sync_interval, t=t,
+                    mode=wl.mode, nbits=wl.nbits, flags=wl.flags, sync_interval=wl.sync_interval, t=t,
                     grads=grads, theta=theta, m=m, want_outputs=False)
         if t >= warmup:
             times.append(time.perf_counter() - t0)
@@ -291,7 +307,7 @@ def run_gpu(args, wl: synth.Workload):
         for i in range(W):
             synth.fill_grad_(grads[s][i], wl, s, i)
     gptrs = [[g.data_ptr() for g in grads[s]] for s in range(nsets)]
-    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd, wl.mode,
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd, wl.mode | wl.flags,
                           wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16, wl.sync_interval)
     lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
     stream = torch.cuda.current_stream(dev)
@@ -397,10 +413,10 @@ def run_gpu(args, wl: synth.Workload):
             "workers": W,
             "params": d,
             "tensors": len(wl.layout),
-            "mode": "sign+majority" if wl.mode == 0 else f"L1 n={wl.nbits} + int sum",
+            "mode": mode_label(wl),
             "grad_dtype": wl.grad,
             "arithmetic": "f32 update vector, momentum and theta (one rounding per operation); integer vote / code sums; u32 packed wire",
-            "sync": "wte every step" if wl.sync_interval else "none",
+            "sync": sync_label(wl),
             "parallelism": f"replicas x{ws} (no inter-GPU exchange)",
             "l2": "flushed between timed steps" if flush else f"inputs larger than L2 ({ws_bytes / 1e9:.1f} GB moved per step)",
         },

@@ -98,12 +98,27 @@ __device__ __forceinline__ void aggregate8(const StepArgs& a, int64_t e0, int* a
     }
 }
 
-// Update direction u from the aggregate: the global sign (a tie gives tie_u),
-// or agg / W for the D-Lion average.
-__device__ __forceinline__ float direction(const StepArgs& a, int agg)
+// D-Lion average: u = RN(agg / W).  A vote sum takes only the 2W + 1 values
+// -W..W, so each block tabulates the quotients once (one division per entry)
+// instead of dividing per element, which made the average's reduce
+// compute-bound.
+constexpr int kAvgTab = 2 * LIONCUB_MAX_WORKERS + 1;
+
+__device__ __forceinline__ void fill_avg_table(const StepArgs& a, float* tab)
 {
     if (a.average)
-        return __fdiv_rn(static_cast<float>(agg), static_cast<float>(a.W));
+        for (int k = threadIdx.x; k <= 2 * a.W; k += blockDim.x)
+            tab[k] = __fdiv_rn(static_cast<float>(k - a.W), static_cast<float>(a.W));
+}
+
+// Update direction u from the aggregate: the global sign (a tie gives tie_u),
+// or agg / W for the D-Lion average (from the block's table).
+__device__ __forceinline__ float direction(const StepArgs& a, int agg, const float* avg_tab)
+{
+    if (a.average) {
+        const int k = agg + a.W;
+        return in_bounds(a, k >= 0 && k <= 2 * a.W) ? avg_tab[k] : 0.0f;
+    }
     return agg > 0 ? 1.0f : (agg < 0 ? -1.0f : a.tie_u);
 }
 
@@ -116,6 +131,9 @@ __device__ __forceinline__ float lion_apply(float theta, float u, float lr, floa
 template <int NB>
 __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
 {
+    __shared__ float avg_tab[kAvgTab];
+    fill_avg_table(a, avg_tab);
+    __syncthreads();
     const int64_t e0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kVec;
     if (e0 >= a.d)
         return;
@@ -128,7 +146,7 @@ __global__ void __launch_bounds__(256) k_reduce_apply(const StepArgs a)
     load_f32(a.theta, e0, valid, th);
 #pragma unroll
     for (int j = 0; j < kVec; ++j)
-        th[j] = lion_apply(th[j], direction(a, agg[j]), a.lr, a.wd);
+        th[j] = lion_apply(th[j], direction(a, agg[j], avg_tab), a.lr, a.wd);
     store_f32(a.theta, e0, valid, th);
 }
 
@@ -202,7 +220,9 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
         if (valid[q] > 0)
             load_f32(a.theta, e0, valid[q], th[q]);
     }
-    __syncthreads();  // the barrier is initialised before anyone polls it
+    __shared__ float avg_tab[kAvgTab];
+    fill_avg_table(a, avg_tab);
+    __syncthreads();  // the barrier is initialised (and the table filled) before anyone polls it
     const uint32_t b = smem_addr(&bar);
     if (!wait_phase0(b)) {
         if (threadIdx.x == 0)
@@ -231,7 +251,7 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
         }
 #pragma unroll
         for (int j = 0; j < kVec; ++j)
-            th[q][j] = lion_apply(th[q][j], direction(a, agg[j]), a.lr, a.wd);
+            th[q][j] = lion_apply(th[q][j], direction(a, agg[j], avg_tab), a.lr, a.wd);
         store_f32(a.theta, blk0 + q * kGroupElems + static_cast<int64_t>(threadIdx.x) * kVec, valid[q], th[q]);
     }
 }

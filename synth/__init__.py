@@ -2,9 +2,9 @@
 
 Holds none of the optimizer's arithmetic.  It provides
 
-* the parameter layouts of the benchmarked models (GPT-2 shapes), as
-  (name, offset, numel, flags) tensors of one flat vector;
-* the five workload configurations (workers, layout, gradient distribution,
+* the parameter layouts of the pages' models (GPT-2 shapes; ViT-B/16 and
+  DeiT-Tiny), as (name, offset, numel, flags) tensors of one flat vector;
+* the workload configurations (workers, layout, gradient distribution,
   compression mode, hyper-parameters, step count);
 * a counter-based GPU generator (``synth.cu``) for gradients and initial
   parameters, so each (seed, step, worker) stream is reproducible and the
@@ -14,7 +14,7 @@ Holds none of the optimizer's arithmetic.  It provides
 
 Gradients follow the workloads' stated distributions: N(0, 1e-3^2) fp32 for
 the flat 1M-element case, 1e-3 * Student-t(nu) rounded to bf16 for the GPT
-layouts (nu = 3, or nu = 2.5 with 0.1% of entries scaled by 100), matching
+and ViT layouts (nu = 3, or nu = 2.5 with 0.1% of entries scaled by 100), matching
 the heavy-tailed, Laplace-like update statistics reported in "Lion Cub:
 Minimizing Communication Overhead in Distributed Lion" (Fig. 3 caption).
 """
@@ -67,6 +67,31 @@ def gpt2_layout(d_model: int, n_layer: int, vocab: int = 50257, n_ctx: int = 102
     return out
 
 
+def vit_layout(d_model: int, n_layer: int, n_classes: int, img: int = 224, patch: int = 16, in_ch: int = 3,
+               mlp_ratio: int = 4, sync=()):
+    """Flat ViT / DeiT parameter layout (timm order): patch projection (w, b),
+    class token, position embedding ((img/patch)^2 + 1 positions); per block
+    norm1 (w, b), attn.qkv (w, b), attn.proj (w, b), norm2 (w, b), mlp.fc1
+    (w, b), mlp.fc2 (w, b); the final norm (w, b); the classification head
+    (w, b), last, so that its bias (n_classes elements, often not a multiple
+    of 32) is the ragged tail.  ``sync`` names the flagged tensors."""
+    D, H = d_model, mlp_ratio * d_model
+    n_pos = (img // patch) ** 2 + 1
+    shapes = [("patch_embed.w", D * in_ch * patch * patch), ("patch_embed.b", D), ("cls_token", D),
+              ("pos_embed", n_pos * D)]
+    for b in range(n_layer):
+        p = f"blocks{b}."
+        shapes += [(p + "norm1.w", D), (p + "norm1.b", D), (p + "attn.qkv.w", 3 * D * D), (p + "attn.qkv.b", 3 * D),
+                   (p + "attn.proj.w", D * D), (p + "attn.proj.b", D), (p + "norm2.w", D), (p + "norm2.b", D),
+                   (p + "mlp.fc1.w", H * D), (p + "mlp.fc1.b", H), (p + "mlp.fc2.w", D * H), (p + "mlp.fc2.b", D)]
+    shapes += [("norm.w", D), ("norm.b", D), ("head.w", n_classes * D), ("head.b", n_classes)]
+    out, off = [], 0
+    for name, n in shapes:
+        out.append((name, off, n, SYNC_M if name in sync else 0))
+        off += n
+    return out
+
+
 def flat_layout(d: int):
     return [("flat", 0, d, 0)]
 
@@ -102,6 +127,7 @@ class Workload:
     wd: float = 0.1
     theta_range: float = 0.05
     seed: int = 0
+    flags: int = 0       # mode flags OR'ed into the mode: 0x100 tie alternation, 0x200 D-Lion average
     notes: str = field(default="")
 
     @property
@@ -122,6 +148,16 @@ def workloads():
                     "bf16", ("t", 3.0, 1e-3, 0.0, 1.0), 0, 1, 20, sync_interval=1),
         5: Workload(5, "gpt2-xl-like-1.3B-w8-l1n2", 8, gpt2_layout(2048, 24, untied_head=True), "bf16",
                     ("t", 3.0, 1e-3, 0.0, 1.0), 1, 2, 10),
+        # the pages' vision models, beyond the five configurations above:
+        # ViT-B/16 on ImageNet with the D-Lion average aggregation, and
+        # DeiT-Tiny fine-tuned on CIFAR-100 with input-embedding and head
+        # momentum synchronized
+        6: Workload(6, "vit-b16-86M-w8-dlion-avg", 8, vit_layout(768, 12, 1000), "bf16",
+                    ("t", 3.0, 1e-3, 0.0, 1.0), 0, 1, 20, flags=0x200),
+        7: Workload(7, "deit-tiny-5.5M-w8-l1n4-embed-head-sync", 8,
+                    vit_layout(192, 12, 100, sync=("patch_embed.w", "patch_embed.b", "cls_token", "pos_embed",
+                                                   "head.w", "head.b")),
+                    "bf16", ("t", 3.0, 1e-3, 0.0, 1.0), 1, 4, 20, sync_interval=1),
     }
 
 

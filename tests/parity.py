@@ -104,6 +104,7 @@ def run_parity(wl: synth.Workload, pieces, steps: int, *, mode_flags: int = 0, s
     m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
     grads = [torch.empty(d, dtype=gdt, device=dev) for _ in range(W)]
 
+    mode_flags |= wl.flags
     h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
                           wl.mode | mode_flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
                           wl.sync_interval)
@@ -281,6 +282,7 @@ def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_
     synth.fill_theta_(theta, wl)
     m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
     grads = [torch.empty(d, dtype=gdt, device=dev) for _ in range(W)]
+    mode_flags |= wl.flags
     h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
                           wl.mode | mode_flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
                           wl.sync_interval)

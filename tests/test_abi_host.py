@@ -169,8 +169,12 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 
 @pytest.mark.parametrize("key,d,K", [(1, 1_048_576, 1), (2, 124_439_808, 148), (3, 354_823_168, 292),
-                                     (4, 354_823_168, 292), (5, 1_416_552_448, 293)])
+                                     (4, 354_823_168, 292), (5, 1_416_552_448, 293),
+                                     (6, 86_567_656, 152), (7, 5_543_716, 152)])
 def test_workload_layouts(key, d, K):
+    """Parameter counts: GPT-2 small 124,439,808 and medium 354,823,168
+    (tied heads), the 1.3B layout with an untied head, ViT-B/16 86,567,656
+    (1000 classes), DeiT-Tiny with a 100-class head 5,543,716."""
     wl = synth.workloads()[key]
     assert wl.d == d and len(wl.layout) == K
     off = 0
@@ -178,7 +182,8 @@ def test_workload_layouts(key, d, K):
         assert o == off and o % 32 == 0
         off += n
     flagged = [t[0] for t in wl.layout if t[3]]
-    assert flagged == (["wte"] if key == 4 else [])
+    want = {4: ["wte"], 7: ["patch_embed.w", "patch_embed.b", "cls_token", "pos_embed", "head.w", "head.b"]}
+    assert flagged == want.get(key, [])
 
 
 def test_bench_byte_model():

@@ -83,6 +83,25 @@ def test_workload5_xl_l1_n2():
     print(rep)
 
 
+def test_workload6_vit_b16_dlion_average():
+    """ViT-B/16 (86,567,656 parameters, ImageNet head) with the D-Lion
+    average aggregation: patch projection, position embedding, one block's
+    attention and MLP weights, the head and its ragged 1000-element bias."""
+    wl = WL[6]
+    assert wl.flags == lc.FLAG_AVERAGE
+    pieces = _names(wl, "patch_embed.w", "cls_token", "pos_embed", "blocks5.attn.qkv.w", "blocks5.mlp.fc2.w",
+                    "norm.b", "head.w", "head.b")
+    parity.run_parity(wl, pieces, wl.steps)
+
+
+def test_workload7_deit_tiny_l1_embedding_head_sync():
+    """DeiT-Tiny with a 100-class head, 4-bit codes, the input embedding
+    (patch projection, class token, position embedding) and the head's
+    momentum synchronized every step: every tensor, whole."""
+    wl = WL[7]
+    parity.run_parity(wl, parity.tensor_pieces(wl.layout, {n for (n, _, _, _) in wl.layout}), wl.steps)
+
+
 @pytest.mark.parametrize("key,names,steps", [
     (3, ("wte",), 2),
     (4, ("wte",), 3),
@@ -276,7 +295,7 @@ def _run_gpu(wl, steps, start=0, state=None, flags=0):
         theta, m = state
     grads = [torch.empty(d, dtype=synth.grad_dtype(wl), device=dev) for _ in range(W)]
     h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
-                          wl.mode | flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
+                          wl.mode | wl.flags | flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
                           wl.sync_interval)
     m1 = None
     try:
