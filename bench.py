@@ -615,7 +615,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(synth.workloads()))
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(synth.workloads()),
+                    help="workload: " + "; ".join(f"{k} = {w.name}" for k, w in sorted(synth.workloads().items())))
     ap.add_argument("--impl", default="lioncub", choices=["lioncub", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
