@@ -54,13 +54,13 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "aaff01b04ec58e36", "m1_finalize": "aaff01b04ec58e36", "reduce_apply": "b33f05b058ff3387"},
+    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "5c0b4a54ecbc6a93", "m1_finalize": "5c0b4a54ecbc6a93", "reduce_apply": "b33f05b058ff3387"},
     "gpt2-small-124M-w8-sign": {"compress": 10021207851, "reduce_apply": 1057754880},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041085867, "m1_finalize": 11115349, "compress": 29790421717, "reduce_apply": 4201522261},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041053611, "m1_finalize": 11113984, "compress": 29791595179, "reduce_apply": 4201389440},
     "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57373891200, "reduce_apply": 3485637888},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016455467, "m1_finalize": 44290091, "compress": 116178687360, "reduce_apply": 14107258667},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016613163, "m1_finalize": 44289536, "compress": 116178673664, "reduce_apply": 14106446805},
     "vit-b16-86M-w8-dlion-avg": {"compress": 6953046187, "reduce_apply": 717670016},
-    "deit-tiny-5.5M-w8-l1n4-embed-head-sync": {"m1_partial": 266411221, "m1_finalize": 195157, "compress": 400234539, "reduce_apply": 44369664},
+    "deit-tiny-5.5M-w8-l1n4-embed-head-sync": {"m1_partial": 266409003, "m1_finalize": 198869, "compress": 400149632, "reduce_apply": 44369152},
 }
 
 

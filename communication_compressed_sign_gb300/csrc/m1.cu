@@ -8,7 +8,9 @@
 // hi/lo pair carrying ~48 significant bits; TwoSum per element), reduced over
 // the warp with shuffles and over the 8 warps in a fixed order, and stores
 // the (hi, lo) pair.  Looping over the workers inside the block amortizes the
-// block's start-up and its serial final merge over W tiles' worth of data.
+// block's start-up and its serial final merge over W tiles' worth of data;
+// layouts with few tiles take one block per (tile, worker) instead, which
+// computes the same pairs.
 // GB300 runs fp64 at a small fraction of its fp32 rate, so a per-element fp64
 // add would cap this pass below memory speed; the pair keeps the per-tile sum
 // accurate to far below one fp32 ulp of the mean.
@@ -29,6 +31,51 @@
 namespace lc {
 namespace {
 
+// The element group of this thread in the block's tile (valid = 0..8).
+__device__ __forceinline__ int tile_group(const StepArgs& a, const Tile& tl, int64_t& e0)
+{
+    e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
+        valid = 0;
+    return valid;
+}
+
+// Compensated sum of |c| over worker i's part of the tile: per thread in
+// element order, a fixed xor-butterfly per warp, then thread 0 merges the 8
+// warps in order (after the barrier) and stores the pair.  `slot` holds the
+// warp sums; every thread of the block takes part.
+template <typename GT>
+__device__ __forceinline__ void tile_partial(const StepArgs& a, int i, int64_t e0, int valid, float2* slot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float hi = 0.0f, lo = 0.0f;
+    if (valid > 0) {
+        float g[kVec], m[kVec];
+        load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            if (j < valid)
+                cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+        const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
+        cacc_merge(hi, lo, ohi, olo);
+    }
+    if (lane == 0)
+        slot[warp] = make_float2(hi, lo);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float h = slot[0].x, l = slot[0].y;
+        for (int w = 1; w < kThreads / 32; ++w)
+            cacc_merge(h, l, slot[w].x, slot[w].y);
+        a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
+    }
+}
+
 template <typename GT>
 __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
 {
@@ -37,40 +84,23 @@ __global__ void __launch_bounds__(kThreads) k_m1_partial(const StepArgs a)
     // barrier of worker i + 1, and slot (i & 1) is rewritten only at i + 2.
     __shared__ float2 red[2][kThreads / 32];
     const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
-    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
-    const int64_t left = tl.start + tl.len - e0;
-    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
-    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
-        valid = 0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t e0;
+    const int valid = tile_group(a, tl, e0);
+    for (int i = 0; i < a.W; ++i)
+        tile_partial<GT>(a, i, e0, valid, red[i & 1]);
+}
 
-    for (int i = 0; i < a.W; ++i) {
-        float hi = 0.0f, lo = 0.0f;
-        if (valid > 0) {
-            float g[kVec], m[kVec];
-            load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
-#pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (j < valid)
-                    cacc_add(hi, lo, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
-            const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
-            cacc_merge(hi, lo, ohi, olo);
-        }
-        float2* slot = red[i & 1];
-        if (lane == 0)
-            slot[warp] = make_float2(hi, lo);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float h = slot[0].x, l = slot[0].y;
-            for (int w = 1; w < kThreads / 32; ++w)
-                cacc_merge(h, l, slot[w].x, slot[w].y);
-            a.partials[static_cast<int64_t>(i) * a.ntiles + blockIdx.x] = make_float2(h, l);
-        }
-    }
+// Small layouts (fewer tiles than a few waves of blocks): one block per
+// (tile, worker) instead, so the grid still fills the SMs.  Each block runs
+// exactly one iteration of the loop above, so the partials are bit-identical.
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) k_m1_partial_tw(const StepArgs a)
+{
+    __shared__ float2 red[kThreads / 32];
+    const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
+    int64_t e0;
+    const int valid = tile_group(a, tl, e0);
+    tile_partial<GT>(a, blockIdx.y, e0, valid, red);
 }
 
 // One block per (worker, tensor): thread t merges tiles t, t + 256, ... of
@@ -112,11 +142,23 @@ __global__ void __launch_bounds__(kFinalThreads) k_m1_finalize(const StepArgs a)
 
 }  // namespace
 
+// Below this many tiles the worker-loop grid would be a few waves at most.
+constexpr int64_t kSmallLayoutTiles = 8192;
+
 cudaError_t launch_m1_partial(const StepArgs& a, int grad_dtype, cudaStream_t s)
 {
     if (a.ntiles == 0)
         return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(a.ntiles)), block(kThreads);
+    const dim3 block(kThreads);
+    if (a.ntiles < kSmallLayoutTiles) {
+        const dim3 grid(static_cast<unsigned>(a.ntiles), static_cast<unsigned>(a.W));
+        if (grad_dtype == LIONCUB_GRAD_BF16)
+            k_m1_partial_tw<__nv_bfloat16><<<grid, block, 0, s>>>(a);
+        else
+            k_m1_partial_tw<float><<<grid, block, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    const dim3 grid(static_cast<unsigned>(a.ntiles));
     if (grad_dtype == LIONCUB_GRAD_BF16)
         k_m1_partial<__nv_bfloat16><<<grid, block, 0, s>>>(a);
     else
