@@ -199,6 +199,23 @@ def test_bench_byte_model():
     assert abs(b / W[5].d - (8 * 6 + 8 * (2 + 8 + 0.25) + 8 * 0.25 + 8)) < 1e-3
 
 
+def test_bench_labels_and_vision_byte_model():
+    """The bench's mode and sync labels come from the workload; the byte
+    model covers the D-Lion average (a sign-mode step) and L1 with sync."""
+    import bench
+    W = synth.workloads()
+    assert bench.mode_label(W[2]) == "sign+majority"
+    assert bench.mode_label(W[3]) == "L1 n=4 + int sum"
+    assert bench.mode_label(W[6]) == "sign + D-Lion average"
+    assert bench.sync_label(W[2]) == "none"
+    assert bench.sync_label(W[4]) == "wte every step"
+    assert bench.sync_label(W[7]).startswith("patch_embed.w, patch_embed.b, cls_token, pos_embed, head.w, head.b")
+    b = bench.step_bytes(W[6])
+    assert abs(b / W[6].d - (8 * (2 + 8 + 1 / 8) + 8 / 8 + 8)) < 1e-3
+    b = bench.step_bytes(W[7])
+    assert abs(b / W[7].d - (8 * 6 + 8 * (2 + 8 + 0.5) + 8 * 0.5 + 8)) < 1e-3
+
+
 def test_header_constants_match_binding(lc):
     """Every LIONCUB_* enum value of the header equals the binding's constant."""
     with open(os.path.join(ROOT, "include", "lioncub.h")) as f:
