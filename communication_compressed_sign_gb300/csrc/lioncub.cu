@@ -309,6 +309,20 @@ void prof_end(lioncub_t h, int slot, cudaStream_t s)
         cudaEventRecord(h->prof_events[2 * slot + 1], s);
 }
 
+// One kernel launch of a step: an NVTX range named for the kernel, the
+// profiling events around it, and the fault-injection check before it.
+template <typename Launch>
+cudaError_t step_launch(lioncub_t h, int kernel, const char* name, cudaStream_t s, Launch&& launch)
+{
+    NvtxRange range(name);
+    const int slot = prof_begin(h, kernel, s);
+    cudaError_t e = injected_launch_fault(h);
+    if (e == cudaSuccess)
+        e = launch();
+    prof_end(h, slot, s);
+    return e;
+}
+
 }  // namespace
 
 namespace lc {
@@ -539,35 +553,21 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
     if (h->prof_this_call)
         --h->prof_steps_left;
     cudaError_t e;
-    int slot;
     if (l1) {
-        slot = prof_begin(h, LIONCUB_KERNEL_M1, s);
-        e = injected_launch_fault(h);
-        if (e == cudaSuccess)
-            e = lc::launch_m1_partial(a, h->grad_dtype, s);
-        prof_end(h, slot, s);
+        e = step_launch(h, LIONCUB_KERNEL_M1, "m1_partial", s,
+                        [&] { return lc::launch_m1_partial(a, h->grad_dtype, s); });
         if (e != cudaSuccess)
             return cuda_fail(h, e, "m1_partial launch");
-        slot = prof_begin(h, LIONCUB_KERNEL_M1_FINAL, s);
-        e = injected_launch_fault(h);
-        if (e == cudaSuccess)
-            e = lc::launch_m1_finalize(a, s);
-        prof_end(h, slot, s);
+        e = step_launch(h, LIONCUB_KERNEL_M1_FINAL, "m1_finalize", s, [&] { return lc::launch_m1_finalize(a, s); });
         if (e != cudaSuccess)
             return cuda_fail(h, e, "m1_finalize launch");
     }
-    slot = prof_begin(h, LIONCUB_KERNEL_COMPRESS, s);
-    e = injected_launch_fault(h);
-    if (e == cudaSuccess)
-        e = lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s);
-    prof_end(h, slot, s);
+    e = step_launch(h, LIONCUB_KERNEL_COMPRESS, "compress", s,
+                    [&] { return lc::launch_compress(a, h->grad_dtype, l1 ? 1 : 0, s); });
     if (e != cudaSuccess)
         return cuda_fail(h, e, "compress launch");
-    slot = prof_begin(h, LIONCUB_KERNEL_REDUCE_APPLY, s);
-    e = injected_launch_fault(h);
-    if (e == cudaSuccess)
-        e = lc::launch_reduce_apply(a, l1 ? 1 : 0, s);
-    prof_end(h, slot, s);
+    e = step_launch(h, LIONCUB_KERNEL_REDUCE_APPLY, "reduce_apply", s,
+                    [&] { return lc::launch_reduce_apply(a, l1 ? 1 : 0, s); });
     if (e != cudaSuccess)
         return cuda_fail(h, e, "reduce_apply launch");
     h->t += 1;
