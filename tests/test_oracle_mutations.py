@@ -51,6 +51,16 @@ MUTATIONS = [
      "float s = 0.0f;\n        for (int j = 1; j < W; ++j)"),
     ("sync_one_step_early", "(t + 1) % sync_interval == 0", "t % sync_interval == 0"),
     ("bf16_widening_wrong", "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+    # the step's orchestration
+    ("vote_skips_last_worker", "    for (int i = 0; i < W; ++i) {\n        uint32_t bit = (words[i][e / 32]",
+     "    for (int i = 0; i < W - 1; ++i) {\n        uint32_t bit = (words[i][e / 32]"),
+    ("code_sum_skips_last_worker", "    for (int i = 0; i < W; ++i) {\n        int32_t f =",
+     "    for (int i = 0; i < W - 1; ++i) {\n        int32_t f ="),
+    ("update_vector_from_worker_0_gradient", "float g = load_grad(grads[i], grad_dtype, off + e);",
+     "float g = load_grad(grads[0], grad_dtype, off + e);"),
+    ("momentum_from_worker_0_gradient", "m[i][e] = lco_momentum(m[i][e], load_grad(grads[i], grad_dtype, e),",
+     "m[i][e] = lco_momentum(m[i][e], load_grad(grads[0], grad_dtype, e),"),
+    ("m1_over_part_of_the_tensor", "float m1 = lco_m1(c, n);", "float m1 = lco_m1(c, (n + 1) / 2);"),
     # diagnostics
     ("worker_std_sample_variance", "return sqrtf(v / (float)W);", "return sqrtf(v / (float)(W - 1 > 0 ? W - 1 : 1));"),
     ("worker_std_mean_wrong", "float mean = s / (float)W;", "float mean = s / (float)(W + 1);"),
