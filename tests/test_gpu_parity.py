@@ -411,8 +411,8 @@ def test_profile_counts_launches():
 # diagnostics (sign match / flip, ties, momentum spread)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("mode,nbits,flags", [(0, 1, 0), (0, 1, lc.FLAG_TIE_ALTERNATE), (1, 2, 0), (1, 4, 0),
-                                              (1, 8, 0)])
+@pytest.mark.parametrize("mode,nbits,flags", [(0, 1, 0), (0, 1, lc.FLAG_TIE_ALTERNATE), (0, 1, lc.FLAG_AVERAGE),
+                                              (1, 2, 0), (1, 4, 0), (1, 8, 0)])
 def test_diagnose_small(mode, nbits, flags):
     layout = _multi_layout(sync=False)
     wl = _small(synth.layout_total(layout), 6, "bf16", mode, nbits, layout=layout)
