@@ -262,6 +262,10 @@ def oracle_rate_probe(wl: synth.Workload) -> float:
     return times[0] / dsub
 
 
+# Arm CPU part numbers (/proc/cpuinfo "CPU part") of the hosts this runs on
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2 (NVIDIA Grace)", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1"}
+
+
 def cpu_info():
     model = "unknown"
     try:
@@ -270,6 +274,7 @@ def cpu_info():
                 low = line.lower()
                 if low.startswith("model name") or low.startswith("cpu part"):
                     model = line.split(":", 1)[1].strip()
+                    model = ARM_PARTS.get(model.lower(), model)
                     break
     except OSError:
         pass
