@@ -43,6 +43,8 @@ struct StepArgs {
     float* m1;                  // W x K (L1 mode)
     float* inv;                 // W x K: RN(qmax / M1), 0 where M1 == 0 (L1 mode)
     int* status;                // device status word: non-zero after a bounded wait gave up
+    uint32_t first_wait_polls;  // fault injection: >0 caps the staged reduce's first wait at this
+                                // many non-blocking polls (0: the normal bounded wait)
     int W;
     int K;
     int nbits;

@@ -80,6 +80,9 @@ struct lioncub_s {
     // report an error instead of running (0 = off)
     int64_t fail_alloc_at = 0, alloc_count = 0;
     int64_t fail_launch_at = 0, launch_count = 0;
+    // fault injection: the staged reduce's first wait gives up after this
+    // many non-blocking polls (0 = off)
+    uint32_t wait_polls = 0;
 
     // profiling
     int prof_steps_left = 0;   // steps still to record
@@ -94,8 +97,9 @@ struct lioncub_s {
 
 namespace {
 
-// Message of the last failed lioncub_create on this thread (no handle exists
-// to hold it).
+// Message of the last failed handle-less call on this thread (lioncub_create,
+// lioncub_host_alloc, lioncub_sign_step_noalloc): no handle exists to hold
+// it.  Each of those calls clears it when it succeeds.
 thread_local std::string g_create_err;
 
 int fail(lioncub_t h, int code, const char* fmt, ...)
@@ -265,6 +269,7 @@ StepArgs make_args(lioncub_t h, const void* const* grads)
     a.m1 = h->m1;
     a.inv = h->inv;
     a.status = h->status;
+    a.first_wait_polls = h->wait_polls;
     a.W = h->W;
     a.K = h->K;
     a.nbits = h->nbits;
@@ -469,6 +474,8 @@ int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_tensor* layou
 
     h->fail_alloc_at = env_index("LIONCUB_FAIL_ALLOC");
     h->fail_launch_at = env_index("LIONCUB_FAIL_LAUNCH");
+    const int64_t polls = env_index("LIONCUB_WAIT_POLLS");
+    h->wait_polls = static_cast<uint32_t>(polls > 0xffff ? 0xffff : polls);
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = guarded_alloc(h, &h->wire, static_cast<size_t>(W) * h->wire_stride + 4);
     if (e == cudaSuccess) e = dev_alloc(h, &h->tiles, tiles.size());
@@ -667,6 +674,7 @@ int lioncub_host_alloc(void** out, size_t bytes)
     if (!out)
         return LIONCUB_ERR_ARG;
     *out = nullptr;
+    g_create_err.clear();
     if (bytes == 0)
         return LIONCUB_OK;
     const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocPortable | cudaHostAllocMapped);

@@ -183,6 +183,18 @@ __device__ __forceinline__ bool wait_phase0(uint32_t b)
     return ok != 0;
 }
 
+// The same with at most `polls` non-blocking tests: the fault-injection
+// stand-in for a wait that runs out (test_wait returns at once, so a block
+// that has just issued its copies gives up before they can have landed).
+__device__ __forceinline__ bool test_phase0(uint32_t b, uint32_t polls)
+{
+    uint32_t ok = 0;
+    for (uint32_t it = 0; it < polls && !ok; ++it)
+        asm volatile("{\n .reg .pred P;\n mbarrier.test_wait.parity.shared::cta.b64 P, [%1], 0;\n selp.u32 %0, 1, 0, P;\n}"
+                     : "=r"(ok) : "r"(b) : "memory");
+    return ok != 0;
+}
+
 template <int NB>
 __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
 {
@@ -224,10 +236,10 @@ __global__ void __launch_bounds__(256) k_reduce_apply_staged(const StepArgs a)
     fill_avg_table(a, avg_tab);
     __syncthreads();  // the barrier is initialised (and the table filled) before anyone polls it
     const uint32_t b = smem_addr(&bar);
-    if (!wait_phase0(b)) {
+    if (!(a.first_wait_polls ? test_phase0(b, a.first_wait_polls) : wait_phase0(b))) {
         if (threadIdx.x == 0)
             atomicOr(a.status, kStatusWaitTimeout);
-        wait_phase0(b);  // drain this block's copies before leaving
+        wait_phase0(b);  // drain this block's copies (full bounded wait) before leaving
         return;
     }
     using T = typename WireChunk<NB>::T;

@@ -63,7 +63,14 @@
  *                          cudaErrorLaunchOutOfResources without launching;
  *   LIONCUB_POISON_GUARD=1 one byte of the guard band after the wire buffer is
  *                          overwritten at creation, so the next status export
- *                          reports LIONCUB_STATUS_GUARD.
+ *                          reports LIONCUB_STATUS_GUARD;
+ *   LIONCUB_WAIT_POLLS=k   the first wait of the staged reduce (for the bulk
+ *                          copies of its wire bytes) gives up after k
+ *                          non-blocking polls (k <= 65535) instead of its
+ *                          normal bound, as a wait that runs out would: the
+ *                          block sets LIONCUB_STATUS_WAIT_TIMEOUT, still waits
+ *                          (with the normal bound) for its own copies to land,
+ *                          and returns without updating its part of theta.
  */
 #ifndef LIONCUB_H
 #define LIONCUB_H
@@ -181,6 +188,9 @@ LIONCUB_API int lioncub_create(lioncub_t* out, int64_t d, int W, const lioncub_t
                    int grad_dtype, int sync_interval);
 
 /*
+ * Source: [DL] "Approach" (each worker keeps its own Lion momentum; the
+ * parameters are shared) and [LC] "What carries the argument" (m_{i,t-1} in
+ * the update vector of worker i).
  * Bind the optimizer state: theta (d fp32, device) and m[0..W-1] (W device
  * pointers to d fp32 each; the host array is read during the call only).
  * The caller owns the memory and keeps it alive while the handle uses it.
@@ -252,7 +262,10 @@ LIONCUB_API int lioncub_set_lr(lioncub_t h, float lr);
 LIONCUB_API int lioncub_get_step(lioncub_t h, int64_t* t);
 LIONCUB_API int lioncub_set_step(lioncub_t h, int64_t t);
 
-/* Words per worker of the wire buffer: ceil(d/32) in sign mode, ceil(d*n/32)
+/* Source: [LC] "What carries the argument" (signs packed as 0/1) and the
+ * Fig. 1 / Fig. 8 captions (1-bit and p-bit containers): the size of what one
+ * worker would send.
+ * Words per worker of the wire buffer: ceil(d/32) in sign mode, ceil(d*n/32)
  * in L1 mode; -1 for a NULL handle. */
 LIONCUB_API int64_t lioncub_wire_words(lioncub_t h);
 
@@ -297,8 +310,14 @@ LIONCUB_API int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_
 LIONCUB_API int lioncub_profile(lioncub_t h, int max_steps);
 LIONCUB_API int lioncub_profile_read(lioncub_t h, int kernel, double* total_ms, int64_t* launches);
 
-/* Message for the last error on h (never NULL; "" when none).  With h ==
- * NULL: the message of the last failed lioncub_create on this thread. */
+/* Source: none on the pages (they define no interface); error reporting
+ * follows the ownership rule above -- the caller owns its buffers and the
+ * stream, the library owns its scratch and its messages.
+ * Message for the last error on h (never NULL; "" when none).  The string
+ * belongs to the library and stays valid until the next call on h.  With
+ * h == NULL: the message of the last failed handle-less call on this thread
+ * (lioncub_create, lioncub_host_alloc, lioncub_sign_step_noalloc); each of
+ * those clears it when it succeeds, so read it right after a non-OK return. */
 LIONCUB_API const char* lioncub_last_error(lioncub_t h);
 /* Static name of a LIONCUB_* return code. */
 LIONCUB_API const char* lioncub_strerror(int code);
@@ -324,17 +343,28 @@ LIONCUB_API const char* lioncub_strerror(int code);
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * Its first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the array: each call rewrites
- * every word it reads, so nothing needs clearing, but calls whose kernels
- * overlap on the GPU (other streams, other threads) race on it.  Errors:
- * ERR_ARG, ERR_ALIGN, ERR_CUDA (messages via lioncub_last_error(NULL)).
+ * before any stream capture.  Under CUDA's lazy module loading that first
+ * lookup is also what loads the array, i.e. when its 16 MiB are taken from
+ * the device: a caller that must not allocate later makes one call with
+ * d == 0 (and valid, aligned pointers) on each device while it initialises;
+ * that call does the set-up, launches nothing and returns LIONCUB_OK, and
+ * later calls allocate nothing.  All calls share the array: each call
+ * rewrites every word it reads, so nothing needs clearing, but calls whose
+ * kernels overlap on the GPU (other streams, other threads) race on it.
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_CUDA (messages via
+ * lioncub_last_error(NULL), which the call clears when it starts).  In the
+ * bounds-checked build (a debugging aid) each call first reads back, with a
+ * synchronous copy, a status word that the previous calls' kernels set on an
+ * out-of-range index, and returns ERR_CUDA if it is set.
  */
 enum { LIONCUB_NOALLOC_MAX_WORDS = 4194304 };
 LIONCUB_API int lioncub_sign_step_noalloc(int64_t d, int W, float beta1, float beta2, float lr, float wd,
                                           int64_t t, int grad_dtype, const void* const* grads, float* theta,
                                           float* const* m, lioncub_stream_t stream);
 
-/* Free the handle's scratch and events.  Synchronizes the device first, so
+/* Source: [DL] "Approach" (the per-worker state is the caller's: theta and
+ * m stay with the caller, only the library's own scratch is released).
+ * Free the handle's scratch and events.  Synchronizes the device first, so
  * no enqueued step still uses the scratch.  NULL is a no-op. */
 LIONCUB_API void lioncub_destroy(lioncub_t h);
 

@@ -4,7 +4,11 @@ Allocation and launch failures come from the library's fault-injection
 environment variables (LIONCUB_FAIL_ALLOC / LIONCUB_FAIL_LAUNCH): the failing
 call is never made, an error code is returned in its place.  A corrupted
 guard band is planted by a host-issued memset at creation
-(LIONCUB_POISON_GUARD).  Nothing here faults, traps or hangs the device.
+(LIONCUB_POISON_GUARD).  The one device wait (the staged reduce's bounded
+wait for its bulk copies) is made to give up early by LIONCUB_WAIT_POLLS,
+which replaces it with a few non-blocking polls; the block still drains its
+copies with the normal bounded wait before it leaves.  Nothing here faults,
+traps or hangs the device.
 
 Checked: every allocation of lioncub_create can fail cleanly (ERR_OOM, no
 leak, the library still usable); a failed staging allocation of the
@@ -12,7 +16,8 @@ host-buffer step leaves the handle usable and a retry computes the same
 result; a launch that fails before the compress kernel leaves theta and m
 untouched, so a retry is bit-exact with a run that never failed; a failure
 of the last launch keeps the step counter and theta; the guard-band check
-reports a planted overrun through the status word.
+reports a planted overrun through the status word; a wait that runs out is
+reported through the status word and leaves the device usable.
 """
 import pytest
 
@@ -268,3 +273,39 @@ def test_guard_check_reports_a_planted_overrun(monkeypatch, mode, nbits):
             assert _status(h) == (lc.STATUS_GUARD if poison else 0)
         finally:
             lc.lioncub_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# the bounded device wait
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 4)])
+def test_wait_timeout_is_reported(monkeypatch, mode, nbits):
+    """The staged reduce's wait for its bulk copies is made to run out
+    (LIONCUB_WAIT_POLLS=1: one non-blocking poll right after the copies are
+    issued, long before they can land): the step still returns and the device
+    stays usable, the blocks that gave up drain their copies and leave, and
+    the status word reports LIONCUB_STATUS_WAIT_TIMEOUT.  A handle created
+    without the hook then matches the oracle."""
+    wl = _wl(1 << 20, 8, mode, nbits)  # 256 staged blocks
+    monkeypatch.setenv("LIONCUB_WAIT_POLLS", "1")
+    st = _State(wl)
+    h = _create(wl)
+    monkeypatch.delenv("LIONCUB_WAIT_POLLS")
+    try:
+        st.bind(h)
+        theta0, m0 = st.snapshot()
+        st.fill(0)
+        st.step(h)  # returns; the kernel's blocks give up and drain
+        assert lc.lioncub_get_step(h) == 1
+        theta1, m1 = st.snapshot()
+        status = _status(h)
+        assert status & lc.STATUS_WAIT_TIMEOUT, status
+        assert status & ~lc.STATUS_WAIT_TIMEOUT == 0, status
+        assert not _equal_bits(m1[0], m0[0])  # the compress pass ran before the reduce gave up
+        # theta is invalid for this step: blocks that gave up left their part unchanged
+        assert int((theta1.view(torch.int32) == theta0.view(torch.int32)).sum()) > 0
+    finally:
+        lc.lioncub_destroy(h)
+    torch.cuda.synchronize()
+    parity.run_parity(_wl(70_001, 8, mode, nbits), parity.tensor_pieces(synth.flat_layout(70_001), {"flat"}), 2)
