@@ -16,7 +16,17 @@
 // loaded holds those 16 MiB until the process exits.  Host code may not use
 // the array's name as a device address (it is a host-side stand-in), so the
 // first call on each device looks the address up with cudaGetSymbolAddress
-// while that device is current and caches it; later calls reuse it.
+// while that device is current and caches it; later calls reuse it.  With
+// lazy module loading that first lookup is also what loads this file's
+// module and reserves the 16 MiB, so a caller that must not allocate later
+// makes one call with d == 0 (and valid pointers) on each device while it is
+// initialising: that call does the set-up and launches nothing.
+//
+// In the bounds-checked build (a debugging aid) the kernels record an index
+// outside its buffer, or a bounded wait that gave up, in a second file-scope
+// word; each call first reads that word back (synchronously) and fails if a
+// previous call's kernels set it.  Ordinary builds pass no status word and
+// never read it.
 //
 // All calls share the one array.  Each call writes every word it later reads
 // (the compress kernel writes all ceil(d/32) words of every worker before the
@@ -40,10 +50,13 @@ using lc::kTile;
 using lc::kVec;
 
 __device__ __align__(256) uint32_t g_noalloc_wire[LIONCUB_NOALLOC_MAX_WORDS];
+// status bits of the bounds-checked build (LIONCUB_STATUS_*); unused otherwise
+__device__ int g_noalloc_status;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_wire_addr[kMaxDevices] = {};
+void* g_status_addr[kMaxDevices] = {};
 
 // The sign-mode compression of one flat tensor, one block per (tile,
 // worker): tile b covers elements [b*2048, min(d, (b+1)*2048)), so no tile
@@ -54,7 +67,10 @@ __global__ void __launch_bounds__(kThreads) k_compress_sign_flat(const lc::StepA
     const int i = blockIdx.y;
     const int64_t e0 = static_cast<int64_t>(blockIdx.x) * kTile + static_cast<int64_t>(threadIdx.x) * kVec;
     const int64_t left = a.d - e0;
-    const int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    // checked builds: the group's word lies inside the worker's row
+    if (valid > 0 && !lc::in_bounds(a, (e0 >> 5) < a.wire_stride && i < a.W))
+        valid = 0;
     const int lane = threadIdx.x & 31;
     float g[kVec], m[kVec];
     if (valid > 0) {
@@ -83,9 +99,9 @@ __global__ void __launch_bounds__(kThreads) k_compress_sign_flat(const lc::StepA
         lc::store_f32(a.m[i], e0, valid, m);
 }
 
-// Device address of g_noalloc_wire on the current device (looked up once per
-// device, with that device current).
-cudaError_t wire_address(void** out)
+// Device addresses of g_noalloc_wire and g_noalloc_status on the current
+// device (looked up once per device, with that device current).
+cudaError_t static_addresses(void** wire, int** status)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -96,12 +112,17 @@ cudaError_t wire_address(void** out)
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_wire_addr[dev]) {
         void* p = nullptr;
+        void* q = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_wire);
+        if (e == cudaSuccess)
+            e = cudaGetSymbolAddress(&q, g_noalloc_status);
         if (e != cudaSuccess)
             return e;
+        g_status_addr[dev] = q;
         g_wire_addr[dev] = p;
     }
-    *out = g_wire_addr[dev];
+    *wire = g_wire_addr[dev];
+    *status = static_cast<int*>(g_status_addr[dev]);
     return cudaSuccess;
 }
 
@@ -117,6 +138,7 @@ extern "C" int lioncub_sign_step_noalloc(int64_t d, int W, float beta1, float be
                                          int64_t t, int grad_dtype, const void* const* grads, float* theta,
                                          float* const* m, lioncub_stream_t stream)
 {
+    lc::set_handleless_error("");
     if (d < 0 || W < 1 || W > LIONCUB_MAX_WORKERS || t < 0)
         return fail(LIONCUB_ERR_ARG, "noalloc step: bad sizes (d >= 0, 1 <= W <= LIONCUB_MAX_WORKERS, t >= 0)");
     if (grad_dtype != LIONCUB_GRAD_BF16 && grad_dtype != LIONCUB_GRAD_F32)
@@ -137,13 +159,24 @@ extern "C" int lioncub_sign_step_noalloc(int64_t d, int W, float beta1, float be
         if ((reinterpret_cast<uintptr_t>(grads[i]) | reinterpret_cast<uintptr_t>(m[i])) & 15u)
             return fail(LIONCUB_ERR_ALIGN, "noalloc step: a gradient or momentum pointer is not 16-byte aligned");
     }
-    if (d == 0)
-        return LIONCUB_OK;
-
+    // set-up (first call on this device): look up the static arrays, which
+    // also loads this file's module; a d == 0 call stops right after it
     void* wire = nullptr;
-    cudaError_t e = wire_address(&wire);
+    int* status = nullptr;
+    cudaError_t e = static_addresses(&wire, &status);
     if (e != cudaSuccess)
         return fail(LIONCUB_ERR_CUDA, "noalloc step: cudaGetSymbolAddress failed");
+    if constexpr (lc::kBoundsCheck) {
+        int bad = 0;
+        e = cudaMemcpy(&bad, status, sizeof bad, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess)
+            return fail(LIONCUB_ERR_CUDA, "noalloc step: reading the status word failed");
+        if (bad != 0)
+            return fail(LIONCUB_ERR_CUDA, "noalloc step: a previous call's kernels set the status word "
+                                          "(bounds-checked build)");
+    }
+    if (d == 0)
+        return LIONCUB_OK;
 
     lc::StepArgs a;
     memset(&a, 0, sizeof a);
@@ -152,6 +185,7 @@ extern "C" int lioncub_sign_step_noalloc(int64_t d, int W, float beta1, float be
         a.m[i] = m[i];
     }
     a.theta = theta;
+    a.status = lc::kBoundsCheck ? status : nullptr;
     a.wire = static_cast<uint32_t*>(wire);
     a.wire_stride = stride;
     a.d = d;
