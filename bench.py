@@ -7,8 +7,10 @@ One step = one pass of the whole path over one batch of synthetic gradients:
 update vectors, compression (packed signs or L1 codes, with the M1 pass),
 the W-way vote or integer sum, the global sign and the theta update, the
 momentum update and the selective momentum sync.  The default workload is
-GPT-2 small (124,439,808 parameters), W = 8 workers, bf16 gradients
-1e-3 * Student-t(3), 1-bit signs with majority vote.
+the largest one that fits one GPU: a GPT-2-XL-like layout with an untied
+head (1,416,552,448 parameters), W = 8 workers, bf16 gradients
+1e-3 * Student-t(3), 2-bit L1 codes with the integer sum (about 198 GB of
+HBM traffic per step; theta and 8 momenta are 51 GB resident).
 
 Metric: parameter-elements per second per step (d / step time), whole job.
 Inputs are far larger than the 129 MB L2 for every GPT workload (11-200 GB
@@ -38,29 +40,30 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 5
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+# GB300 HBM3e bandwidth as the vendor states it (8 TB/s per GPU), for context
+# next to the measured copy bandwidth
+NOMINAL_HBM_GBS = 8000.0
 
-# DRAM bytes per step of each kernel (dram__bytes_read.sum + dram__bytes_write.sum,
-# summed over the kernel's launches in one step), from one-pass ncu captures of
-# the full workloads (profiles/traffic_full_workloads.md).  Each entry holds
-# for the kernel sources it was taken on: `traffic` is reported only while the
-# fingerprint of those sources still matches.
+# DRAM bytes per parameter of each kernel in one step: dram__bytes_read.sum +
+# dram__bytes_write.sum over the kernel's launches of one step, divided by the
+# parameters of the case, from one ncu capture of a small case of each
+# workload (a slice of its layout, a few GB on the device, inputs still far
+# larger than L2).  Every kernel streams each parameter's bytes once, so its
+# traffic grows in proportion to the parameters; the bench scales the figure
+# by the full workload's parameter count.  An entry holds for the kernel
+# sources it was taken on: traffic is reported only while the fingerprint of
+# those sources still matches.
 KERNEL_SOURCES = {
     "compress": ("compress.cu", "device_common.cuh", "internal.h"),
     "m1_partial": ("m1.cu", "device_common.cuh", "internal.h"),
     "m1_finalize": ("m1.cu", "device_common.cuh", "internal.h"),
     "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
 }
-MEASURED_TRAFFIC = {
-    "fingerprints": {"compress": "9991e336ebae2eff", "m1_partial": "5c0b4a54ecbc6a93", "m1_finalize": "5c0b4a54ecbc6a93", "reduce_apply": "b33f05b058ff3387"},
-    "gpt2-small-124M-w8-sign": {"compress": 10021207851, "reduce_apply": 1057754880},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 17041053611, "m1_finalize": 11113984, "compress": 29791595179, "reduce_apply": 4201389440},
-    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 57373891200, "reduce_apply": 3485637888},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 68016613163, "m1_finalize": 44289536, "compress": 116178673664, "reduce_apply": 14106446805},
-    "vit-b16-86M-w8-dlion-avg": {"compress": 6953046187, "reduce_apply": 717670016},
-    "deit-tiny-5.5M-w8-l1n4-embed-head-sync": {"m1_partial": 266409003, "m1_finalize": 198869, "compress": 400149632, "reduce_apply": 44369152},
+MEASURED_TRAFFIC_PER_PARAM = {
+    "fingerprints": {},
 }
 
 
@@ -73,15 +76,17 @@ def source_fingerprint(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str, kernel: str):
-    """DRAM bytes per step of `kernel` on `workload`, or None when no capture
-    exists or the kernel's sources changed since it was taken."""
-    entry = MEASURED_TRAFFIC.get(workload, {})
+def measured_traffic(wl: synth.Workload, kernel: str):
+    """DRAM bytes per step of `kernel` on workload `wl` (the small-case figure
+    per parameter times wl.d), or None when no capture exists for the
+    workload or the kernel's sources changed since it was taken."""
+    base = wl.name.split("[", 1)[0]
+    entry = MEASURED_TRAFFIC_PER_PARAM.get(base, {})
     if kernel not in entry or kernel not in KERNEL_SOURCES:
         return None
-    if MEASURED_TRAFFIC["fingerprints"].get(kernel) != source_fingerprint(kernel):
+    if MEASURED_TRAFFIC_PER_PARAM["fingerprints"].get(kernel) != source_fingerprint(kernel):
         return None
-    return entry[kernel]
+    return int(round(entry[kernel] * wl.d))
 
 
 # ---------------------------------------------------------------------------
@@ -369,7 +374,7 @@ def run_gpu(args, wl: synth.Workload):
         if n:
             per_kernel[name] = {"ms_per_step": tot / args.steps, "launches_per_step": n / args.steps,
                                 "share": None, "alg_bytes": kb.get(name, 0),
-                                "traffic": measured_traffic(wl.name, name)}
+                                "traffic": measured_traffic(wl, name)}
     ksum = sum(v["ms_per_step"] for v in per_kernel.values()) or 1.0
     for v in per_kernel.values():
         v["share"] = v["ms_per_step"] / ksum
@@ -427,10 +432,10 @@ def run_gpu(args, wl: synth.Workload):
         },
         "hbm": {"alg_bytes_per_step": ws_bytes, "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac_of_measured" if peak_kind == "measured" else "frac_of_fallback": step_gbs / peak,
-                "frac_of_nominal_7900": step_gbs / 7900.0},
+                "frac_of_nominal_8000": step_gbs / NOMINAL_HBM_GBS},
         "roofline": {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": measured_traffic(wl.name, top),
+                     "traffic": measured_traffic(wl, top),
                      "alg_bytes": per_kernel[top]["alg_bytes"]},
         "kernels": per_kernel,
         "gpu_launches": recorded,
@@ -602,17 +607,19 @@ def run_reference(args, wl: synth.Workload):
     }
 
 
-def truncated(wl: synth.Workload, limit: int) -> synth.Workload:
-    """The workload restricted to its leading tensors (at least one), about
-    `limit` parameters; the name records the cut."""
+def truncated(wl: synth.Workload, limit: int, skip: int = 0) -> synth.Workload:
+    """The workload restricted to consecutive tensors: after the first `skip`
+    tensors, the leading ones (at least one) up to about `limit` parameters,
+    re-based to offset 0; the name records the cut."""
     keep, total = [], 0
-    for t in wl.layout:
-        if keep and total + t[2] > limit:
+    for (name, _, n, fl) in wl.layout[skip:]:
+        if keep and total + n > limit:
             break
-        keep.append(t)
-        total += t[2]
+        keep.append((name, total, n, fl))
+        total += n
     import dataclasses
-    return dataclasses.replace(wl, layout=keep, name=f"{wl.name}[first {len(keep)} tensors, {total} params]")
+    cut = f"tensors {skip}..{skip + len(keep) - 1}, {total} params"
+    return dataclasses.replace(wl, layout=keep, name=f"{wl.name}[{cut}]")
 
 
 def main(argv=None):
@@ -634,13 +641,15 @@ def main(argv=None):
     ap.add_argument("--nbits", type=int, default=None, help="code width for --mode l1 (2, 4 or 8)")
     ap.add_argument("--layout-limit", type=int, default=0,
                     help="profiling aid: keep only the workload's leading tensors, about this many parameters")
+    ap.add_argument("--skip-tensors", type=int, default=0,
+                    help="profiling aid: with --layout-limit, start after this many tensors")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "lioncub":
         print("note: warm-up raised to 3 steps", file=sys.stderr)
         args.warmup = 3
     wl = synth.workloads()[args.config]
     if args.layout_limit:
-        wl = truncated(wl, args.layout_limit)
+        wl = truncated(wl, args.layout_limit, args.skip_tensors)
     if args.mode is not None:
         import dataclasses
         mode = 0 if args.mode == "sign" else 1
