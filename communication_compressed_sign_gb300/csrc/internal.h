@@ -16,6 +16,10 @@ namespace lc {
 constexpr int kThreads = 256;
 constexpr int kVec = 8;
 constexpr int kTile = kThreads * kVec;
+// Data-parallel exchange: each rank's chunk of the parameter vector is a
+// multiple of this many elements, so a chunk's wire rows start on 16-byte
+// boundaries for every code width and a packed word never spans two chunks.
+constexpr int64_t kDistChunkAlign = 4096;
 
 // One tile: elements [start, start + len); meta = tensor index, with bit 31
 // set when the tensor's momentum is synchronized across workers.
@@ -45,6 +49,13 @@ struct StepArgs {
     int* status;                // device status word: non-zero after a bounded wait gave up
     uint32_t first_wait_polls;  // fault injection: >0 caps the staged reduce's first wait at this
                                 // many non-blocking polls (0: the normal bounded wait)
+    // data-parallel exchange across ranks (lioncub_dist_*); all 0 otherwise
+    int64_t chunk;        // sign mode: elements of each rank's chunk (a multiple of 4096); the
+                          // compress pass then writes its wire words chunk-major (row c*W + i)
+    int64_t chunk_words;  // words per worker and chunk in that layout
+    float* sync_buf;      // new momenta of synchronized tiles, worker-major, sync_slots each:
+                          // written by the compress pass, read (all ranks' workers) by the apply
+    int64_t sync_slots;   // elements per worker in the sync buffers (synchronized tiles x 2048)
     int W;
     int K;
     int nbits;
@@ -88,5 +99,13 @@ cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s);
 cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s);
 cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lioncub_diag* out, cudaStream_t s);
+
+// data-parallel exchange (dist.cu)
+cudaError_t launch_compress_dist(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s);
+cudaError_t launch_owner_reduce(const StepArgs& a, int dir_bits, void* dir, cudaStream_t s);
+cudaError_t launch_code_sum_local(const StepArgs& a, int agg_bytes, void* agg, cudaStream_t s);
+cudaError_t launch_apply_dir(const StepArgs& a, int dir_bits, const void* dir, cudaStream_t s);
+cudaError_t launch_apply_agg(const StepArgs& a, int agg_bytes, const void* agg, cudaStream_t s);
+cudaError_t launch_sync_mean(const StepArgs& a, int W_global, const float* recv, cudaStream_t s);
 
 }  // namespace lc

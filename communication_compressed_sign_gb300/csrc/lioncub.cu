@@ -25,6 +25,7 @@ using lc::Tile;
 // Layouts the language bindings rely on.
 static_assert(sizeof(lioncub_tensor) == 24, "lioncub_tensor must stay 24 bytes");
 static_assert(sizeof(lioncub_diag) == 48, "lioncub_diag must stay 48 bytes");
+static_assert(sizeof(lioncub_dist_plan) == 104, "lioncub_dist_plan must stay 104 bytes");
 static_assert(sizeof(StepArgs) <= 4096, "kernel parameters must fit the classic 4 KB limit");
 static_assert(lc::kStatusWaitTimeout == LIONCUB_STATUS_WAIT_TIMEOUT &&
                   lc::kStatusOutOfBounds == LIONCUB_STATUS_OUT_OF_BOUNDS && lc::kStatusGuard == LIONCUB_STATUS_GUARD,
@@ -91,6 +92,16 @@ struct lioncub_s {
     std::vector<cudaEvent_t> prof_events;  // pairs
     std::vector<int> prof_kernel;
     int prof_used = 0;
+
+    // data-parallel exchange (lioncub_dist_create): this rank's share of the
+    // workers (W above is the local count), the exchange plan and the
+    // caller's exchange buffers
+    bool dist = false;
+    int nranks = 1, rank = 0, W_global = 0;
+    lioncub_dist_plan plan{};
+    void* xbuf[LIONCUB_DIST_BUFFERS] = {};
+    bool xbound = false;
+    int phase = 0;  // the next exchange call: 0 compress, 1 reduce, 2 apply
 
     std::string err;
 };
@@ -542,6 +553,8 @@ int lioncub_step(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
 {
     if (!h)
         return LIONCUB_ERR_ARG;
+    if (h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "a data-parallel handle steps through lioncub_dist_compress/reduce/apply");
     if (!h->bound)
         return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
     if (!grads)
@@ -586,6 +599,8 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
 {
     if (!h)
         return LIONCUB_ERR_ARG;
+    if (h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "a data-parallel handle steps through lioncub_dist_compress/reduce/apply");
     if (!h->bound)
         return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
     if (!grads_host || !theta_host_out)
@@ -666,6 +681,234 @@ int lioncub_step_host(lioncub_t h, const void* const* grads_host, float* theta_h
     if (e != cudaSuccess)
         return cuda_fail(h, e, "theta download");
     ++h->host_calls;
+    return LIONCUB_OK;
+}
+
+int lioncub_dist_plan_make(int64_t d, int W, int nranks, int rank, const lioncub_tensor* layout, int K, int mode,
+                           int nbits, int sync_interval, lioncub_dist_plan* out)
+{
+    if (!out)
+        return LIONCUB_ERR_ARG;
+    std::memset(out, 0, sizeof *out);
+    g_create_err.clear();
+    const int base_mode = mode & 0xff;
+    const bool average = (mode & LIONCUB_FLAG_AVERAGE) != 0;
+    if (d < 0 || W < 1 || W > LIONCUB_MAX_WORKERS || nranks < 1 || nranks > W || W % nranks != 0 || rank < 0 ||
+        rank >= nranks || K < 0 || (K > 0 && !layout))
+        return fail(nullptr, LIONCUB_ERR_ARG,
+                    "bad exchange sizes: d=%lld W=%d nranks=%d rank=%d K=%d (need 1 <= nranks <= W, W %% nranks == 0)",
+                    (long long)d, W, nranks, rank, K);
+    if (base_mode != LIONCUB_MODE_SIGN_MAJORITY && base_mode != LIONCUB_MODE_L1_INTSUM)
+        return fail(nullptr, LIONCUB_ERR_ARG, "unknown mode %d", base_mode);
+    if (base_mode == LIONCUB_MODE_L1_INTSUM && nbits != 2 && nbits != 4 && nbits != 8)
+        return fail(nullptr, LIONCUB_ERR_ARG, "nbits must be 2, 4 or 8 in L1 mode (got %d)", nbits);
+    if (average && W > 127)
+        return fail(nullptr, LIONCUB_ERR_ARG, "the exchanged vote sums of the average are int8: W <= 127");
+    const int W_loc = W / nranks;
+    out->local_workers = W_loc;
+    out->first_worker = rank * W_loc;
+    if (base_mode == LIONCUB_MODE_SIGN_MAJORITY) {
+        const int64_t blocks = (d + lc::kDistChunkAlign - 1) / lc::kDistChunkAlign;
+        const int64_t per = (blocks + nranks - 1) / nranks;
+        out->chunk = (per > 0 ? per : 1) * lc::kDistChunkAlign;
+        out->chunk_words = out->chunk / 32;
+        out->dir_bits = average ? 8 : 2;
+        out->dir_words = out->chunk * out->dir_bits / 32;
+        out->bytes[LIONCUB_DIST_SEND] = static_cast<int64_t>(nranks) * W_loc * out->chunk_words * 4;
+        out->bytes[LIONCUB_DIST_RECV] = static_cast<int64_t>(W) * out->chunk_words * 4;
+        out->bytes[LIONCUB_DIST_DIR_CHUNK] = out->dir_words * 4;
+        out->bytes[LIONCUB_DIST_DIR_ALL] = static_cast<int64_t>(nranks) * out->dir_words * 4;
+    } else {
+        const int qmax = (1 << (nbits - 1)) - 1;
+        out->agg_bytes = (static_cast<int64_t>(W) * qmax <= 127) ? 1 : 4;
+        out->bytes[LIONCUB_DIST_AGG] = (d * out->agg_bytes + 15) / 16 * 16;
+    }
+    if (sync_interval > 0) {
+        int64_t slots = 0;
+        for (int k = 0; k < K; ++k)
+            if (layout[k].flags & LIONCUB_TENSOR_SYNC_M)
+                slots += (layout[k].numel + lc::kTile - 1) / lc::kTile * lc::kTile;
+        out->sync_slots = slots;
+        out->bytes[LIONCUB_DIST_SYNC_SEND] = static_cast<int64_t>(W_loc) * slots * 4;
+        out->bytes[LIONCUB_DIST_SYNC_RECV] = static_cast<int64_t>(W) * slots * 4;
+    }
+    return LIONCUB_OK;
+}
+
+int lioncub_dist_create(lioncub_t* out, int64_t d, int W, int nranks, int rank, const lioncub_tensor* layout, int K,
+                        float beta1, float beta2, float lr, float wd, int mode, int nbits, int grad_dtype,
+                        int sync_interval)
+{
+    if (!out)
+        return LIONCUB_ERR_ARG;
+    *out = nullptr;
+    lioncub_dist_plan plan;
+    int rc = lioncub_dist_plan_make(d, W, nranks, rank, layout, K, mode, nbits, sync_interval, &plan);
+    if (rc != LIONCUB_OK)
+        return rc;
+    rc = lioncub_create(out, d, plan.local_workers, layout, K, beta1, beta2, lr, wd, mode, nbits, grad_dtype,
+                        sync_interval);
+    if (rc != LIONCUB_OK)
+        return rc;
+    lioncub_t h = *out;
+    h->dist = true;
+    h->nranks = nranks;
+    h->rank = rank;
+    h->W_global = W;
+    h->plan = plan;
+    return LIONCUB_OK;
+}
+
+int lioncub_dist_bind_buffers(lioncub_t h, void* const* bufs)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (!h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "not a data-parallel handle (use lioncub_dist_create)");
+    if (!bufs)
+        return fail(h, LIONCUB_ERR_ARG, "bufs is NULL");
+    for (int b = 0; b < LIONCUB_DIST_BUFFERS; ++b) {
+        if (h->plan.bytes[b] > 0 && !bufs[b])
+            return fail(h, LIONCUB_ERR_ARG, "exchange buffer %d is NULL but the plan needs %lld bytes", b,
+                        (long long)h->plan.bytes[b]);
+        if (bufs[b] && !aligned16(bufs[b]))
+            return fail(h, LIONCUB_ERR_ALIGN, "exchange buffer %d is not 16-byte aligned", b);
+    }
+    for (int b = 0; b < LIONCUB_DIST_BUFFERS; ++b)
+        h->xbuf[b] = h->plan.bytes[b] > 0 ? bufs[b] : nullptr;
+    h->xbound = true;
+    h->phase = 0;
+    h->err.clear();
+    return LIONCUB_OK;
+}
+
+namespace {
+
+// Checks shared by the three exchange calls.
+int dist_ready(lioncub_t h, int phase, const char* what)
+{
+    if (!h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "%s: not a data-parallel handle", what);
+    if (!h->bound || !h->xbound)
+        return fail(h, LIONCUB_ERR_STATE, "%s: bind the state and the exchange buffers first", what);
+    if (h->phase != phase)
+        return fail(h, LIONCUB_ERR_STATE, "%s out of order: the next exchange call is %s", what,
+                    h->phase == 0 ? "lioncub_dist_compress" : h->phase == 1 ? "lioncub_dist_reduce"
+                                                                          : "lioncub_dist_apply");
+    return LIONCUB_OK;
+}
+
+// StepArgs of an exchange call: the local workers, and the exchange fields.
+StepArgs dist_args(lioncub_t h, const void* const* grads)
+{
+    StepArgs a = make_args(h, grads);
+    a.sync_slots = h->plan.sync_slots;
+    return a;
+}
+
+}  // namespace
+
+int lioncub_dist_compress(lioncub_t h, const void* const* grads, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    int rc = dist_ready(h, 0, "lioncub_dist_compress");
+    if (rc != LIONCUB_OK)
+        return rc;
+    if (!grads)
+        return fail(h, LIONCUB_ERR_ARG, "grads is NULL");
+    for (int i = 0; i < h->W; ++i) {
+        if (!grads[i])
+            return fail(h, LIONCUB_ERR_ARG, "grads[%d] is NULL", i);
+        if (!aligned16(grads[i]))
+            return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
+    }
+    NvtxRange range("lioncub_dist_compress");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
+    StepArgs a = dist_args(h, grads);
+    a.sync_buf = static_cast<float*>(h->xbuf[LIONCUB_DIST_SYNC_SEND]);
+    if (!l1) {
+        a.wire = static_cast<uint32_t*>(h->xbuf[LIONCUB_DIST_SEND]);
+        a.wire_stride = 0;
+        a.chunk = h->plan.chunk;
+        a.chunk_words = h->plan.chunk_words;
+    }
+    h->prof_this_call = false;
+    cudaError_t e = cudaSuccess;
+    if (l1) {
+        e = step_launch(h, LIONCUB_KERNEL_M1, "m1_partial", s, [&] { return lc::launch_m1_partial(a, h->grad_dtype, s); });
+        if (e == cudaSuccess)
+            e = step_launch(h, LIONCUB_KERNEL_M1_FINAL, "m1_finalize", s, [&] { return lc::launch_m1_finalize(a, s); });
+    }
+    if (e == cudaSuccess)
+        e = step_launch(h, LIONCUB_KERNEL_COMPRESS, "compress_dist", s,
+                        [&] { return lc::launch_compress_dist(a, h->grad_dtype, l1 ? 1 : 0, s); });
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "exchange compress launch");
+    h->phase = 1;
+    return LIONCUB_OK;
+}
+
+int lioncub_dist_reduce(lioncub_t h, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    int rc = dist_ready(h, 1, "lioncub_dist_reduce");
+    if (rc != LIONCUB_OK)
+        return rc;
+    NvtxRange range("lioncub_dist_reduce");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    StepArgs a = dist_args(h, nullptr);
+    cudaError_t e;
+    if (h->mode == LIONCUB_MODE_SIGN_MAJORITY) {
+        // the owner's chunk: W rows of chunk_words received words
+        const int64_t c0 = static_cast<int64_t>(h->rank) * h->plan.chunk;
+        const int64_t len = h->d - c0;
+        a.d = len < 0 ? 0 : (len < h->plan.chunk ? len : h->plan.chunk);
+        a.W = h->W_global;
+        a.wire = static_cast<uint32_t*>(h->xbuf[LIONCUB_DIST_RECV]);
+        a.wire_stride = h->plan.chunk_words;
+        e = step_launch(h, LIONCUB_KERNEL_REDUCE_APPLY, "owner_reduce", s,
+                        [&] { return lc::launch_owner_reduce(a, h->plan.dir_bits, h->xbuf[LIONCUB_DIST_DIR_CHUNK], s); });
+    } else {
+        e = step_launch(h, LIONCUB_KERNEL_REDUCE_APPLY, "code_sum_local", s,
+                        [&] { return lc::launch_code_sum_local(a, h->plan.agg_bytes, h->xbuf[LIONCUB_DIST_AGG], s); });
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "exchange reduce launch");
+    h->phase = 2;
+    return LIONCUB_OK;
+}
+
+int lioncub_dist_apply(lioncub_t h, lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    int rc = dist_ready(h, 2, "lioncub_dist_apply");
+    if (rc != LIONCUB_OK)
+        return rc;
+    NvtxRange range("lioncub_dist_apply");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    StepArgs a = dist_args(h, nullptr);
+    cudaError_t e;
+    if (h->mode == LIONCUB_MODE_SIGN_MAJORITY) {
+        StepArgs b = a;
+        b.W = h->W_global;  // the average's table divides by every worker
+        e = step_launch(h, LIONCUB_KERNEL_REDUCE_APPLY, "apply_dir", s,
+                        [&] { return lc::launch_apply_dir(b, h->plan.dir_bits, h->xbuf[LIONCUB_DIST_DIR_ALL], s); });
+    } else {
+        e = step_launch(h, LIONCUB_KERNEL_REDUCE_APPLY, "apply_agg", s,
+                        [&] { return lc::launch_apply_agg(a, h->plan.agg_bytes, h->xbuf[LIONCUB_DIST_AGG], s); });
+    }
+    if (e == cudaSuccess && a.sync_now && h->plan.sync_slots > 0)
+        e = step_launch(h, LIONCUB_KERNEL_COMPRESS, "sync_mean", s, [&] {
+            return lc::launch_sync_mean(a, h->W_global, static_cast<const float*>(h->xbuf[LIONCUB_DIST_SYNC_RECV]), s);
+        });
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "exchange apply launch");
+    h->t += 1;
+    h->phase = 0;
     return LIONCUB_OK;
 }
 
@@ -767,6 +1010,8 @@ int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_de
 {
     if (!h)
         return LIONCUB_ERR_ARG;
+    if (h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "diagnostics need every worker on one GPU (not a data-parallel handle)");
     if (!h->bound)
         return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
     if (!grads || !out_dev)

@@ -46,7 +46,13 @@ EXPORTED = (
     "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read",
     "lioncub_last_error", "lioncub_strerror", "lioncub_destroy", "lioncub_sign_step_noalloc",
     "lioncub_diagnose", "lioncub_host_alloc", "lioncub_host_free",
+    "lioncub_dist_plan_make", "lioncub_dist_create", "lioncub_dist_bind_buffers", "lioncub_dist_compress",
+    "lioncub_dist_reduce", "lioncub_dist_apply",
 )
+# exchange buffers of the data-parallel step (LIONCUB_DIST_*)
+DIST_SEND, DIST_RECV, DIST_DIR_CHUNK, DIST_DIR_ALL, DIST_AGG, DIST_SYNC_SEND, DIST_SYNC_RECV = range(7)
+DIST_BUFFERS = 7
+DIST_BUFFER_NAMES = ("send", "recv", "dir_chunk", "dir_all", "agg", "sync_send", "sync_recv")
 NOALLOC_MAX_WORDS = 4194304
 
 
@@ -58,6 +64,14 @@ class LionCubError(RuntimeError):
 
 class Tensor(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_int64), ("numel", ctypes.c_int64), ("flags", ctypes.c_uint32)]
+
+
+class DistPlan(ctypes.Structure):
+    """lioncub_dist_plan: where the exchange of one rank puts what."""
+    _fields_ = [("chunk", ctypes.c_int64), ("chunk_words", ctypes.c_int64), ("dir_words", ctypes.c_int64),
+                ("sync_slots", ctypes.c_int64), ("local_workers", ctypes.c_int32),
+                ("first_worker", ctypes.c_int32), ("dir_bits", ctypes.c_int32), ("agg_bytes", ctypes.c_int32),
+                ("bytes", ctypes.c_int64 * 7)]
 
 
 _lock = threading.Lock()
@@ -102,6 +116,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.lioncub_host_alloc.restype = i32
         L.lioncub_host_free.argtypes = [vp]
         L.lioncub_host_free.restype = None
+        L.lioncub_dist_plan_make.argtypes = [i64, i32, i32, i32, vp, i32, i32, i32, i32, ctypes.POINTER(DistPlan)]
+        L.lioncub_dist_create.argtypes = [ctypes.POINTER(vp), i64, i32, i32, i32, vp, i32, f32, f32, f32, f32,
+                                          i32, i32, i32, i32]
+        L.lioncub_dist_bind_buffers.argtypes = [vp, vp]
+        L.lioncub_dist_compress.argtypes = [vp, vp, vp]
+        L.lioncub_dist_reduce.argtypes = [vp, vp]
+        L.lioncub_dist_apply.argtypes = [vp, vp]
+        for name in ("lioncub_dist_plan_make", "lioncub_dist_create", "lioncub_dist_bind_buffers",
+                     "lioncub_dist_compress", "lioncub_dist_reduce", "lioncub_dist_apply"):
+            getattr(L, name).restype = i32
         for name in ("lioncub_create", "lioncub_bind_state", "lioncub_step", "lioncub_step_host",
                      "lioncub_set_lr", "lioncub_get_step", "lioncub_set_step",
                      "lioncub_debug_export", "lioncub_profile", "lioncub_profile_read"):
@@ -256,6 +280,51 @@ def lioncub_sign_step_noalloc(d: int, W: int, beta1: float, beta2: float, lr: fl
                                           ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), theta_ptr,
                                           ctypes.cast(_ptrs(m_ptrs), ctypes.c_void_p), stream or None)
     _check(rc, None)
+
+
+def _layout_arg(layout):
+    if layout:
+        arr = (Tensor * len(layout))(*[Tensor(int(o), int(n), int(f)) for (o, n, f) in layout])
+        return arr, ctypes.cast(arr, ctypes.c_void_p), len(layout)
+    return None, None, 0
+
+
+def lioncub_dist_plan_make(d: int, W: int, nranks: int, rank: int, layout, mode: int, nbits: int,
+                           sync_interval: int) -> DistPlan:
+    """The exchange plan of one rank (host arithmetic only; no device needed)."""
+    keep, lp, K = _layout_arg(layout)
+    plan = DistPlan()
+    _check(load().lioncub_dist_plan_make(d, W, nranks, rank, lp, K, mode, nbits, sync_interval,
+                                         ctypes.byref(plan)), None)
+    return plan
+
+
+def lioncub_dist_create(d: int, W: int, nranks: int, rank: int, layout, beta1: float, beta2: float, lr: float,
+                        wd: float, mode: int, nbits: int, grad_dtype: int, sync_interval: int) -> int:
+    keep, lp, K = _layout_arg(layout)
+    h = ctypes.c_void_p()
+    rc = load().lioncub_dist_create(ctypes.byref(h), d, W, nranks, rank, lp, K, beta1, beta2, lr, wd, mode, nbits,
+                                    grad_dtype, sync_interval)
+    _check(rc, None)
+    return h.value
+
+
+def lioncub_dist_bind_buffers(h: int, ptrs) -> None:
+    """ptrs: DIST_BUFFERS device addresses (0 where the plan needs none)."""
+    assert len(ptrs) == DIST_BUFFERS
+    _check(load().lioncub_dist_bind_buffers(h, ctypes.cast(_ptrs([p or 0 for p in ptrs]), ctypes.c_void_p)), h)
+
+
+def lioncub_dist_compress(h: int, grad_ptrs, stream: int = 0) -> None:
+    _check(load().lioncub_dist_compress(h, ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), stream or None), h)
+
+
+def lioncub_dist_reduce(h: int, stream: int = 0) -> None:
+    _check(load().lioncub_dist_reduce(h, stream or None), h)
+
+
+def lioncub_dist_apply(h: int, stream: int = 0) -> None:
+    _check(load().lioncub_dist_apply(h, stream or None), h)
 
 
 def lioncub_destroy(h: int) -> None:

@@ -323,6 +323,118 @@ LIONCUB_API const char* lioncub_last_error(lioncub_t h);
 LIONCUB_API const char* lioncub_strerror(int code);
 
 /*
+ * ---- Data-parallel exchange: the W workers spread over several ranks ----
+ *
+ * Source: [LC] the quoted body text on the implementation (1-bit Lion Cub
+ * exchanges its packed signs with an AlltoAll; the 4-bit and wider variants
+ * sum their codes with an AllReduce), "What carries the argument" (a 1-bit
+ * compressed allreduce tailored to majority voting: each worker's packed
+ * signs are split into chunks, the owner of a chunk takes its vote, the
+ * result is gathered back; momentum averaged on the input-embedding and
+ * output layers) and the Fig. 1 / Fig. 8 captions.
+ *
+ * N ranks (one GPU each) hold W/N workers each -- rank r the global workers
+ * r*W/N .. (r+1)*W/N - 1 -- and each a copy of theta.  The library does
+ * every arithmetic step in its kernels; the caller's collective library
+ * (NCCL, for example through torch.distributed) moves the exchange buffers
+ * between the three calls of a step, on the same stream:
+ *
+ *   sign mode:  lioncub_dist_compress      (wire words -> SEND, chunk-major)
+ *               all-to-all SEND -> RECV    (equal segments of bytes[SEND]/N:
+ *                                           segment r goes to rank r, and the
+ *                                           segment from rank s lands at
+ *                                           segment s of RECV)
+ *               lioncub_dist_reduce        (vote of this rank's chunk ->
+ *                                           DIR_CHUNK)
+ *               allgather DIR_CHUNK -> DIR_ALL (rank order)
+ *               [sync step: allgather SYNC_SEND -> SYNC_RECV (rank order)]
+ *               lioncub_dist_apply         (theta, synchronized momenta)
+ *   L1 mode:    lioncub_dist_compress      (M1, codes of the local workers)
+ *               lioncub_dist_reduce        (their code sum -> AGG, int8 or
+ *                                           int32 per element, see agg_bytes)
+ *               allreduce (sum) of AGG in place
+ *               [sync step: allgather SYNC_SEND -> SYNC_RECV]
+ *               lioncub_dist_apply
+ *
+ * A sync step is one with sync_interval > 0 and (t+1) % sync_interval == 0
+ * for the handle's step counter t before lioncub_dist_apply.  Every rank ends
+ * the step with the same theta, and each rank's momenta equal those of the
+ * same workers in a single-GPU lioncub_step over all W workers, bit for bit:
+ * integer sums do not depend on their order, and the momentum average sums
+ * the gathered momenta in worker order on every rank.
+ *
+ * Sign mode: rank r owns elements [r*chunk, min(d, (r+1)*chunk)); SEND holds
+ * N*(W/N) rows of chunk_words words, row (c*(W/N) + i) carrying local worker
+ * i's packed signs of chunk c (LSB first, as the single-GPU wire); RECV holds
+ * W rows (global worker order) of this rank's chunk.  DIR_CHUNK packs one
+ * field per element of the chunk: dir_bits = 2, the two's-complement
+ * direction -1, 0 or +1 after the tie rule; dir_bits = 8 (with
+ * LIONCUB_FLAG_AVERAGE), the vote sum itself.  DIR_ALL is N such chunks.
+ * L1 mode: AGG holds d sums of agg_bytes (1 when W*qmax <= 127, else 4).
+ * SYNC_SEND holds, per local worker, the new momenta of the synchronized
+ * tensors in layout order, each padded to a multiple of 2048 elements
+ * (sync_slots per worker); SYNC_RECV holds W such rows in worker order.
+ */
+enum {
+    LIONCUB_DIST_SEND = 0,
+    LIONCUB_DIST_RECV = 1,
+    LIONCUB_DIST_DIR_CHUNK = 2,
+    LIONCUB_DIST_DIR_ALL = 3,
+    LIONCUB_DIST_AGG = 4,
+    LIONCUB_DIST_SYNC_SEND = 5,
+    LIONCUB_DIST_SYNC_RECV = 6,
+    LIONCUB_DIST_BUFFERS = 7
+};
+
+typedef struct {
+    int64_t chunk;          /* sign mode: elements per rank's chunk (a multiple of 4096) */
+    int64_t chunk_words;    /* sign mode: words per worker and chunk (chunk / 32)        */
+    int64_t dir_words;      /* sign mode: words of one chunk's directions               */
+    int64_t sync_slots;     /* elements per worker in the sync buffers                  */
+    int32_t local_workers;  /* W / nranks                                               */
+    int32_t first_worker;   /* rank * W / nranks                                        */
+    int32_t dir_bits;       /* sign mode: 2, or 8 with the average                      */
+    int32_t agg_bytes;      /* L1 mode: 1 (int8) or 4 (int32)                            */
+    int64_t bytes[LIONCUB_DIST_BUFFERS]; /* size of each exchange buffer; 0 = unused     */
+} lioncub_dist_plan;
+
+/*
+ * The exchange plan of rank `rank` of `nranks` for a step of W workers on d
+ * parameters (arguments as lioncub_create; W % nranks == 0).  Host
+ * arithmetic only: no CUDA call, no device needed.  Errors: ERR_ARG.
+ */
+LIONCUB_API int lioncub_dist_plan_make(int64_t d, int W, int nranks, int rank, const lioncub_tensor* layout,
+                                       int K, int mode, int nbits, int sync_interval, lioncub_dist_plan* out);
+
+/*
+ * A handle for rank `rank` of `nranks`, holding the W/nranks local workers
+ * (arguments otherwise as lioncub_create).  lioncub_bind_state then takes
+ * W/nranks momenta.  The single-GPU lioncub_step, lioncub_step_host and
+ * lioncub_diagnose refuse such a handle (ERR_STATE).
+ */
+LIONCUB_API int lioncub_dist_create(lioncub_t* out, int64_t d, int W, int nranks, int rank,
+                                    const lioncub_tensor* layout, int K, float beta1, float beta2, float lr,
+                                    float wd, int mode, int nbits, int grad_dtype, int sync_interval);
+
+/*
+ * Bind the exchange buffers: bufs[LIONCUB_DIST_BUFFERS] device pointers,
+ * each at least the plan's bytes[b] (NULL where that is 0), 16-byte aligned,
+ * owned by the caller (so that its collective library can register them).
+ * Errors: ERR_STATE (not a data-parallel handle), ERR_ARG, ERR_ALIGN.
+ */
+LIONCUB_API int lioncub_dist_bind_buffers(lioncub_t h, void* const* bufs);
+
+/*
+ * The three launches of a step, in this order (ERR_STATE otherwise), with
+ * the caller's collectives between them as described above.  compress
+ * reads the local gradients (grads: W/nranks device pointers, like
+ * lioncub_step); apply advances the step counter.  None synchronizes.
+ */
+LIONCUB_API int lioncub_dist_compress(lioncub_t h, const void* const* grads, lioncub_stream_t stream);
+LIONCUB_API int lioncub_dist_reduce(lioncub_t h, lioncub_stream_t stream);
+LIONCUB_API int lioncub_dist_apply(lioncub_t h, lioncub_stream_t stream);
+
+/*
  * Allocation-free sign-mode step.  It has no counterpart on the pages: it is
  * for callers that cannot allocate device memory at the time they run a step
  * -- for example an application whose allocator has reserved all device

@@ -34,7 +34,7 @@ def _declared():
 
 def test_header_symbols_exported(lc):
     declared = _declared()
-    assert len(declared) == 18
+    assert len(declared) == 24
     lib = ctypes.CDLL(lc.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name
@@ -239,6 +239,10 @@ def test_header_constants_match_binding(lc):
         "LIONCUB_KERNEL_COUNT": lc.KERNEL_COUNT, "LIONCUB_NOALLOC_MAX_WORDS": lc.NOALLOC_MAX_WORDS,
         "LIONCUB_STATUS_WAIT_TIMEOUT": lc.STATUS_WAIT_TIMEOUT, "LIONCUB_STATUS_OUT_OF_BOUNDS": lc.STATUS_OUT_OF_BOUNDS,
         "LIONCUB_STATUS_GUARD": lc.STATUS_GUARD,
+        "LIONCUB_DIST_SEND": lc.DIST_SEND, "LIONCUB_DIST_RECV": lc.DIST_RECV,
+        "LIONCUB_DIST_DIR_CHUNK": lc.DIST_DIR_CHUNK, "LIONCUB_DIST_DIR_ALL": lc.DIST_DIR_ALL,
+        "LIONCUB_DIST_AGG": lc.DIST_AGG, "LIONCUB_DIST_SYNC_SEND": lc.DIST_SYNC_SEND,
+        "LIONCUB_DIST_SYNC_RECV": lc.DIST_SYNC_RECV, "LIONCUB_DIST_BUFFERS": lc.DIST_BUFFERS,
     }
     assert set(values) == set(expect), set(values) ^ set(expect)
     for name, v in expect.items():
@@ -246,3 +250,20 @@ def test_header_constants_match_binding(lc):
     # struct layouts the binding assumes
     assert ctypes.sizeof(lc.Tensor) == 24
     assert lc.DIAG_BYTES == 48
+    assert ctypes.sizeof(lc.DistPlan) == 104
+
+
+def test_dist_calls_check_their_handle(lc):
+    """The data-parallel calls refuse a NULL handle and bad plans without
+    touching CUDA; a plan is host arithmetic and needs no device."""
+    L = lc.load()
+    assert L.lioncub_dist_compress(None, None, None) == lc.ERR_ARG
+    assert L.lioncub_dist_reduce(None, None) == lc.ERR_ARG
+    assert L.lioncub_dist_apply(None, None) == lc.ERR_ARG
+    assert L.lioncub_dist_bind_buffers(None, None) == lc.ERR_ARG
+    assert L.lioncub_dist_plan_make(100, 4, 2, 0, None, 0, 0, 1, 0, None) == lc.ERR_ARG
+    p = lc.lioncub_dist_plan_make(1 << 20, 8, 4, 3, None, lc.MODE_L1_INTSUM, 4, 0)
+    assert (p.local_workers, p.first_worker, p.agg_bytes) == (2, 6, 1)  # 8 * 7 = 56 fits int8
+    assert p.bytes[lc.DIST_AGG] == 1 << 20 and p.bytes[lc.DIST_SEND] == 0
+    p = lc.lioncub_dist_plan_make(1 << 20, 32, 4, 3, None, lc.MODE_L1_INTSUM, 4, 0)
+    assert p.agg_bytes == 4  # 32 * 7 = 224 does not
