@@ -53,17 +53,23 @@ NOMINAL_HBM_GBS = 8000.0
 # workload (a slice of its layout, a few GB on the device, inputs still far
 # larger than L2).  Every kernel streams each parameter's bytes once, so its
 # traffic grows in proportion to the parameters; the bench scales the figure
-# by the full workload's parameter count.  An entry holds for the kernel
-# sources it was taken on: traffic is reported only while the fingerprint of
-# those sources still matches.
+# by the full workload's parameter count.  Writes read a little low: up to an
+# L2's worth of dirty lines are still in L2 when a launch ends (2-3.5 % of a
+# 3 GB compress launch; about 18 % of the 0.3-0.4 GB reduce launches of the
+# small cases, which makes their scaled figure a lower bound).  An entry
+# holds for the kernel sources it was taken on: traffic is reported only
+# while the fingerprint of those sources still matches.
 KERNEL_SOURCES = {
-    "compress": ("compress.cu", "device_common.cuh", "internal.h"),
+    "compress": ("compress.cu", "compress_common.cuh", "device_common.cuh", "internal.h"),
     "m1_partial": ("m1.cu", "device_common.cuh", "internal.h"),
     "m1_finalize": ("m1.cu", "device_common.cuh", "internal.h"),
-    "reduce_apply": ("reduce_apply.cu", "device_common.cuh", "internal.h"),
+    "reduce_apply": ("reduce_apply.cu", "aggregate.cuh", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC_PER_PARAM = {
-    "fingerprints": {},
+    "fingerprints": {"compress": "de7027d602a8df83", "m1_partial": "3d8735ef82c15b8f", "m1_finalize": "3d8735ef82c15b8f", "reduce_apply": "dd210a47b9a144de"},
+    "gpt2-small-124M-w8-sign": {"compress": 79.4727, "reduce_apply": 7.3645},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 48.1076, "m1_finalize": 0.0317, "compress": 82.526, "reduce_apply": 10.4939},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 48.1096, "m1_finalize": 0.0317, "compress": 80.2218, "reduce_apply": 8.2165},
 }
 
 
@@ -451,6 +457,107 @@ def run_gpu(args, wl: synth.Workload):
     return result if rank == 0 else None
 
 
+def run_gpu_exchange(args, wl: synth.Workload):
+    """The data-parallel exchange: the workload's W workers spread over the N
+    ranks (W/N each, one GPU per rank), every rank with its own theta; a step
+    is the library's three launches with NCCL collectives between them
+    (all-to-all of packed words and allgather of directions in sign mode,
+    allreduce of code sums in L1 mode, allgather of synchronized momenta on
+    sync steps).  The whole job takes one step over d parameters, so value =
+    d / step time and the scaling is strong.  With one process (no torchrun)
+    it runs as a one-rank NCCL group on GPU 0."""
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    from communication_compressed_sign_gb300 import lioncub as lc
+    from communication_compressed_sign_gb300.dist import DistLionCub
+
+    ws, rank, local = dist_env()
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if ws == 1:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            os.environ.setdefault("MASTER_PORT", str(sk.getsockname()[1]))
+        os.environ.setdefault("RANK", "0")
+        os.environ.setdefault("WORLD_SIZE", "1")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(dev)
+    lc.load()
+    d, W = wl.d, wl.W
+    if W % ws:
+        raise SystemExit(f"--exchange needs W ({W}) divisible by the number of ranks ({ws})")
+    gcode = lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16
+    opt = DistLionCub(d, W, synth.abi_layout(wl.layout), beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr, wd=wl.wd,
+                      mode=wl.mode | wl.flags, nbits=wl.nbits, grad_dtype=gcode, sync_interval=wl.sync_interval,
+                      device=dev)
+    Wl, first = opt.plan.local_workers, opt.plan.first_worker
+    theta = torch.empty(d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(Wl)]
+    opt.bind(theta, m)
+    gdt = synth.grad_dtype(wl)
+    grads = [[torch.empty(d, dtype=gdt, device=dev) for _ in range(Wl)] for _ in range(2)]
+    for s in range(2):
+        for i in range(Wl):
+            synth.fill_grad_(grads[s][i], wl, s, first + i)
+    stream = torch.cuda.current_stream(dev)
+    for s in range(args.warmup):
+        opt.step(grads[s % 2], stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        opt.step(grads[s % 2], stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    clk = clocks.stop()
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, dev)
+    moved = {lc.DIST_BUFFER_NAMES[b]: int(opt.plan.bytes[b]) for b in range(lc.DIST_BUFFERS)}
+    # the library's launches in the timed steps: (M1 pass and combine,) compress, reduce, apply, and the
+    # momentum average on sync steps
+    from communication_compressed_sign_gb300.dist import is_sync_step
+    t0 = args.warmup
+    launches = sum((5 if wl.mode == 1 else 3) + (1 if is_sync_step(t0 + s, wl.sync_interval, opt.plan) else 0)
+                   for s in range(args.steps))
+    opt.close()
+    dist.destroy_process_group()
+    if rank != 0:
+        return None
+    return {
+        "metric": "param-elements/s per Lion Cub step (W simulated workers)",
+        "value": d / (ms * 1e-3),
+        "unit": "param-elements/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "strong",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded counter-based Student-t / normal gradients, uniform theta)",
+        "config": {"workload": wl.name, "workers": W, "workers_per_rank": Wl, "params": d, "mode": mode_label(wl),
+                   "sync": sync_label(wl), "grad_dtype": wl.grad,
+                   "parallelism": f"data-parallel exchange over {ws} rank(s): "
+                                  + ("all-to-all of packed signs + allgather of 2-bit directions" if wl.mode == 0
+                                     else "allreduce of integer code sums"),
+                   "exchange_buffer_bytes_per_rank": moved},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+
+
 def run_diagnose(args, wl, h, dev, stream, grad_ptrs):
     """Time lioncub_diagnose (the pages' sign match/flip, tie and momentum
     spread measurements) over the whole workload; report its bandwidth and the
@@ -641,6 +748,9 @@ def main(argv=None):
     ap.add_argument("--nbits", type=int, default=None, help="code width for --mode l1 (2, 4 or 8)")
     ap.add_argument("--layout-limit", type=int, default=0,
                     help="profiling aid: keep only the workload's leading tensors, about this many parameters")
+    ap.add_argument("--exchange", action="store_true",
+                    help="spread the W workers over the ranks and exchange with NCCL (the multi-GPU path) "
+                         "instead of running one replica per GPU")
     ap.add_argument("--skip-tensors", type=int, default=0,
                     help="profiling aid: with --layout-limit, start after this many tensors")
     args = ap.parse_args(argv)
@@ -656,7 +766,12 @@ def main(argv=None):
         nbits = 1 if mode == 0 else (args.nbits or 4)
         wl = dataclasses.replace(wl, mode=mode, nbits=nbits,
                                  name=f"{wl.name}[{'sign' if mode == 0 else f'L1 n={nbits}'}]")
-    res = run_reference(args, wl) if args.impl == "reference" else run_gpu(args, wl)
+    if args.impl == "reference":
+        res = run_reference(args, wl)
+    elif args.exchange:
+        res = run_gpu_exchange(args, wl)
+    else:
+        res = run_gpu(args, wl)
     if res is not None:
         print(json.dumps(res))
 

@@ -22,7 +22,7 @@ def test_reference_arm_json_line():
     assert out["impl"] == "reference"
     assert out["steps"] == 2 and out["warmup"] == 1 and out["higher_is_better"] is True
     assert out["value"] > 0 and out["unit"] == "param-elements/s"
-    assert out["config"]["workload"] == "gpt2-small-124M-w8-sign"
+    assert out["config"]["workload"] == "gpt2-xl-like-1.3B-w8-l1n2"  # the default, largest one-GPU workload
     cb = out["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == out["value"] and cb["sample"]
     assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
