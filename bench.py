@@ -66,10 +66,11 @@ KERNEL_SOURCES = {
     "reduce_apply": ("reduce_apply.cu", "aggregate.cuh", "device_common.cuh", "internal.h"),
 }
 MEASURED_TRAFFIC_PER_PARAM = {
-    "fingerprints": {"compress": "de7027d602a8df83", "m1_partial": "3d8735ef82c15b8f", "m1_finalize": "3d8735ef82c15b8f", "reduce_apply": "dd210a47b9a144de"},
-    "gpt2-small-124M-w8-sign": {"compress": 79.4727, "reduce_apply": 7.3645},
-    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 48.1076, "m1_finalize": 0.0317, "compress": 82.526, "reduce_apply": 10.4939},
-    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 48.1096, "m1_finalize": 0.0317, "compress": 80.2218, "reduce_apply": 8.2165},
+    "fingerprints": {"compress": "05bcd3f2a61840b4", "m1_partial": "3d8735ef82c15b8f", "m1_finalize": "3d8735ef82c15b8f", "reduce_apply": "39b5679b2e040586"},
+    "gpt2-small-124M-w8-sign": {"compress": 79.4703, "reduce_apply": 7.3768},
+    "gpt2-medium-350M-w8-l1n4": {"m1_partial": 48.1079, "m1_finalize": 0.0317, "compress": 82.537, "reduce_apply": 10.514},
+    "gpt2-medium-350M-w16-sign-wte-sync": {"compress": 154.8846, "reduce_apply": 6.2913},
+    "gpt2-xl-like-1.3B-w8-l1n2": {"m1_partial": 48.1092, "m1_finalize": 0.0317, "compress": 80.2149, "reduce_apply": 8.1801},
 }
 
 
@@ -753,6 +754,9 @@ def main(argv=None):
                          "instead of running one replica per GPU")
     ap.add_argument("--skip-tensors", type=int, default=0,
                     help="profiling aid: with --layout-limit, start after this many tensors")
+    ap.add_argument("--sync-names", default="",
+                    help="profiling aid: comma-separated tensors whose momentum is synchronized instead of the "
+                         "workload's own (needs a workload with a sync interval)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "lioncub":
         print("note: warm-up raised to 3 steps", file=sys.stderr)
@@ -760,6 +764,11 @@ def main(argv=None):
     wl = synth.workloads()[args.config]
     if args.layout_limit:
         wl = truncated(wl, args.layout_limit, args.skip_tensors)
+    if args.sync_names:
+        import dataclasses
+        names = set(args.sync_names.split(","))
+        lay = [(n, o, c, synth.SYNC_M if n in names else 0) for (n, o, c, _) in wl.layout]
+        wl = dataclasses.replace(wl, layout=lay, name=f"{wl.name}[sync {args.sync_names}]")
     if args.mode is not None:
         import dataclasses
         mode = 0 if args.mode == "sign" else 1

@@ -55,13 +55,16 @@ __global__ void __launch_bounds__(kThreads, 8) k_compress(const StepArgs a, int6
 // Tiles of synchronized tensors on a sync step: one block per tile, the
 // thread loops over the workers in order, summing their new momenta in
 // registers, and writes the mean to every worker (no extra memory pass).
-// Full groups of 8 elements are software-pipelined: worker i+1's gradients
-// and momenta are requested (as packed vectors) before worker i is computed
-// and stored, so each thread keeps two workers' loads in flight.  The one
-// ragged group at the end of the vector takes the plain loop.
+// Each iteration asks L2 for the gradients and momenta of the worker two
+// ahead (prefetch instructions hold no registers), so the loop's loads
+// mostly hit L2 while DRAM streams the next ones; at 40 registers six blocks
+// fit an SM.  Measured on the 16-worker GPT-2-medium workload against
+// keeping the next worker's loads in registers (63 registers, four blocks):
+// the sync tiles' pass ran about 5 % faster, at the plain tiles' rate.
 template <typename GT, int NB>
-__global__ void __launch_bounds__(kThreads) k_compress_sync(const StepArgs a, int64_t tile0)
+__global__ void __launch_bounds__(kThreads, 6) k_compress_sync(const StepArgs a, int64_t tile0)
 {
+    constexpr int kAhead = 2;
     const int64_t tix = tile0 + blockIdx.x;
     const Tile tl = in_bounds(a, tix < a.ntiles) ? a.tiles[tix] : Tile{0, 0, 0u};
     const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
@@ -76,43 +79,36 @@ __global__ void __launch_bounds__(kThreads) k_compress_sync(const StepArgs a, in
     for (int j = 0; j < kVec; ++j)
         acc[j] = 0.0f;
     if (valid == kVec) {
-        Raw8<GT> cur, nxt;
-        cur.load(a.g[0], a.m[0], e0);
-        for (int i = 0; i < a.W; ++i) {
-            if (i + 1 < a.W)
-                nxt.load(a.g[i + 1], a.m[i + 1], e0);
-            float g[kVec], m[kVec];
-            cur.unpack(g, m);
-            float inv = 0.0f;
-            if constexpr (NB > 1)
-                inv = a.inv[static_cast<int64_t>(i) * a.K + k];
-            const uint64_t bits = compress8<NB>(a, g, m, kVec, inv);
-            store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, kVec, bits);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
-            cur = nxt;
-        }
-    } else {
-        for (int i = 0; i < a.W; ++i) {
-            float g[kVec], m[kVec];
-            if (valid > 0) {
-                load_grad<GT>(a.g[i], e0, valid, g);
-                load_f32(a.m[i], e0, valid, m);
-            } else {
-#pragma unroll
-                for (int j = 0; j < kVec; ++j)
-                    g[j] = m[j] = 0.0f;
+        for (int q = 0; q < kAhead; ++q) {
+            if (q < a.W) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const GT*>(a.g[q]) + e0));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.m[q] + e0));
             }
-            float inv = 0.0f;
-            if constexpr (NB > 1)
-                inv = a.inv[static_cast<int64_t>(i) * a.K + k];
-            const uint64_t bits = compress8<NB>(a, g, m, valid, inv);
-            store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
+        }
+    }
+    for (int i = 0; i < a.W; ++i) {
+        if (valid == kVec && i + kAhead < a.W) {
+            const int q = i + kAhead;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const GT*>(a.g[q]) + e0));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.m[q] + e0));
+        }
+        float g[kVec], m[kVec];
+        if (valid > 0) {
+            load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
+        } else {
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
-                acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
+                g[j] = m[j] = 0.0f;
         }
+        float inv = 0.0f;
+        if constexpr (NB > 1)
+            inv = a.inv[static_cast<int64_t>(i) * a.K + k];
+        const uint64_t bits = compress8<NB>(a, g, m, valid, inv);
+        store_wire<NB>(a.wire + static_cast<int64_t>(i) * a.wire_stride, e0, valid, bits);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            acc[j] = (i == 0) ? m[j] : __fadd_rn(acc[j], m[j]);
     }
     if (valid > 0) {
         const float fw = static_cast<float>(a.W);
