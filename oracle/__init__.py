@@ -47,6 +47,14 @@ class Diag(ctypes.Structure):
 DIAG_FIELDS = ("match", "flip", "dropped", "spurious", "ties", "max_std_m")
 
 
+class QinfDiag(ctypes.Structure):
+    _fields_ = [("match", ctypes.c_int64), ("flip", ctypes.c_int64), ("dropped", ctypes.c_int64),
+                ("spurious", ctypes.c_int64), ("zero_codes", ctypes.c_int64)]
+
+
+QINF_FIELDS = ("match", "flip", "dropped", "spurious", "zero_codes")
+
+
 class Tensor(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_int64), ("numel", ctypes.c_int64), ("flags", ctypes.c_uint32)]
 
@@ -111,6 +119,17 @@ def lib() -> ctypes.CDLL:
             L.lco_classify.restype = i32
             L.lco_diagnose.argtypes = [i64, i32, vp, i32, f32, i32, i32, u32, i64, i32, vp, vp, vp]
             L.lco_diagnose.restype = i32
+            u64 = ctypes.c_uint64
+            L.lco_splitmix64.argtypes = [u64, u64]
+            L.lco_splitmix64.restype = u64
+            L.lco_qinf_uniform.argtypes = [u64, i64, i32, i64]
+            L.lco_qinf_uniform.restype = f32
+            L.lco_maxabs.argtypes = [vp, i64]
+            L.lco_maxabs.restype = f32
+            L.lco_qinf.argtypes = [vp, i64, i32, f32, u64, i64, i32, i64, vp]
+            L.lco_qinf.restype = None
+            L.lco_diagnose_qinf.argtypes = [i64, i32, vp, i32, f32, i32, u32, i64, u64, i64, i32, vp, vp, vp]
+            L.lco_diagnose_qinf.restype = i32
             _lib = L
     return _lib
 
@@ -287,3 +306,45 @@ def diagnose(*, d: int, W: int, layout, beta1: float, mode: int, nbits: int, fla
     if rc != 0:
         raise ValueError(f"oracle diagnose rejected its arguments (rc={rc})")
     return [{f: getattr(o, f) for f in DIAG_FIELDS} for o in out]
+
+
+# ---- Q_inf: max-norm scaling with stochastic rounding -------------------------
+
+def splitmix64(seed: int, k: int) -> int:
+    """Output number k of SplitMix64 started from state `seed`."""
+    return int(lib().lco_splitmix64(seed & (2**64 - 1), k & (2**64 - 1)))
+
+
+def qinf_uniform(seed: int, t: int, worker: int, e: int) -> float:
+    return float(lib().lco_qinf_uniform(seed & (2**64 - 1), t, worker, e))
+
+
+def maxabs(c: np.ndarray) -> np.float32:
+    c = np.ascontiguousarray(c, dtype=np.float32)
+    return np.float32(lib().lco_maxabs(_ptr(c) if c.size else None, c.size))
+
+
+def qinf(c: np.ndarray, nbits: int, *, seed: int, t: int, worker: int, e_first: int = 0,
+         maxabs_value=None) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.float32)
+    if maxabs_value is None:
+        maxabs_value = maxabs(c)
+    out = np.zeros(max(1, c.size), dtype=np.int8)
+    lib().lco_qinf(_ptr(c), c.size, nbits, float(maxabs_value), seed & (2**64 - 1), t, worker, e_first, _ptr(out))
+    return out[: c.size]
+
+
+def diagnose_qinf(*, d: int, W: int, layout, beta1: float, nbits: int, flags: int, t: int, seed: int,
+                  e_base: int, grads, m):
+    """Per-tensor Q_inf comparison (see lioncub_oracle.h); list of dicts with
+    the QINF_FIELDS keys."""
+    gdt = GRAD_BF16 if grads[0].dtype == np.uint16 else GRAD_F32
+    lay, K = layout_array(layout)
+    out = (QinfDiag * max(K, 1))()
+    rc = lib().lco_diagnose_qinf(d, W, ctypes.cast(lay, ctypes.c_void_p) if lay is not None else None, K,
+                                 beta1, nbits, flags, t, seed & (2**64 - 1), e_base, gdt,
+                                 ctypes.cast(_ptr_array(grads), ctypes.c_void_p),
+                                 ctypes.cast(_ptr_array(m), ctypes.c_void_p), ctypes.addressof(out))
+    if rc != 0:
+        raise ValueError(f"oracle Q_inf diagnose rejected its arguments (rc={rc})")
+    return [{f: getattr(o, f) for f in QINF_FIELDS} for o in out]

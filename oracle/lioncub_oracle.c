@@ -435,3 +435,114 @@ done:
     free(col);
     return rc;
 }
+
+/* ---- Q_inf: max-norm scaling with stochastic rounding (see the header) ---- */
+
+uint64_t lco_splitmix64(uint64_t seed, uint64_t k)
+{
+    uint64_t z = seed + (k + 1u) * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+float lco_qinf_uniform(uint64_t seed, int64_t t, int worker, int64_t e)
+{
+    uint64_t k = (((uint64_t)t & 0xffffu) << 48) | ((uint64_t)(unsigned)worker << 40) | (uint64_t)e;
+    uint64_t bits = lco_splitmix64(seed, k) >> 40; /* 24 bits */
+    return (float)bits * (1.0f / 16777216.0f);
+}
+
+float lco_maxabs(const float* c, int64_t n)
+{
+    float mx = 0.0f;
+    for (int64_t e = 0; e < n; ++e)
+        if (fabsf(c[e]) > mx)
+            mx = fabsf(c[e]);
+    return mx;
+}
+
+void lco_qinf(const float* c, int64_t n, int nbits, float maxabs, uint64_t seed, int64_t t, int worker,
+              int64_t e_first, int8_t* q)
+{
+    int qmax = (1 << (nbits - 1)) - 1;
+    float inv = maxabs > 0.0f ? (float)qmax / maxabs : 0.0f;
+    for (int64_t e = 0; e < n; ++e) {
+        float y = fabsf(c[e]) * inv;
+        float fl = floorf(y);
+        float frac = y - fl;
+        float u = lco_qinf_uniform(seed, t, worker, e_first + e);
+        int v = (int)fl + (u < frac ? 1 : 0);
+        if (v > qmax)
+            v = qmax;
+        q[e] = (int8_t)(c[e] < 0.0f ? -v : v);
+    }
+}
+
+int lco_diagnose_qinf(int64_t d, int W, const lco_tensor* layout, int K, float beta1, int nbits, uint32_t flags,
+                      int64_t t, uint64_t seed, int64_t e_base, int grad_dtype, const void* const* grads,
+                      const float* const* m, lco_qinf_diag* out)
+{
+    if (d < 0 || W < 1 || W > 255 || !grads || !m || !out)
+        return -1;
+    if (nbits != 2 && nbits != 4 && nbits != 8)
+        return -1;
+    lco_tensor whole;
+    whole.offset = 0;
+    whole.numel = d;
+    whole.flags = 0;
+    if (!layout || K == 0) {
+        layout = &whole;
+        K = 1;
+    }
+    int64_t maxn = 0;
+    for (int k = 0; k < K; ++k)
+        if (layout[k].numel > maxn)
+            maxn = layout[k].numel;
+    int rc = 0;
+    float* c = (float*)malloc((size_t)(maxn > 0 ? maxn : 1) * sizeof(float));
+    int8_t* q = (int8_t*)malloc((size_t)(maxn > 0 ? maxn : 1) * (size_t)W);
+    float* s = (float*)malloc((size_t)(maxn > 0 ? maxn : 1) * sizeof(float));
+    if (!c || !q || !s) {
+        rc = -2;
+        goto done;
+    }
+    uint32_t dir_flags = flags & ~LCO_FLAG_AVERAGE;
+    for (int k = 0; k < K; ++k) {
+        int64_t off = layout[k].offset, n = layout[k].numel;
+        lco_qinf_diag r;
+        memset(&r, 0, sizeof r);
+        /* each worker: update vector, its max-norm, its Q_inf codes; the
+         * full-precision sum in worker order */
+        for (int i = 0; i < W; ++i) {
+            for (int64_t e = 0; e < n; ++e) {
+                c[e] = lco_update_vector(m[i][off + e], load_grad(grads[i], grad_dtype, off + e), beta1,
+                                         lco_omega(beta1));
+                s[e] = (i == 0) ? c[e] : s[e] + c[e];
+            }
+            lco_qinf(c, n, nbits, lco_maxabs(c, n), seed, t, i, e_base + off, q + (int64_t)i * n);
+        }
+        for (int64_t e = 0; e < n; ++e) {
+            int32_t agg = 0;
+            for (int i = 0; i < W; ++i) {
+                int8_t qi = q[(int64_t)i * n + e];
+                agg += qi;
+                if (qi == 0)
+                    r.zero_codes += 1;
+            }
+            float u_q = sign_of(lco_direction(agg, W, dir_flags, t));
+            switch (lco_classify(u_q, sign_of(s[e]))) {
+            case 0: r.match += 1; break;
+            case 1: r.flip += 1; break;
+            case 2: r.dropped += 1; break;
+            default: r.spurious += 1; break;
+            }
+        }
+        out[k] = r;
+    }
+done:
+    free(c);
+    free(q);
+    free(s);
+    return rc;
+}

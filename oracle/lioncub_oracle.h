@@ -166,6 +166,53 @@ int lco_diagnose(int64_t d, int W, const lco_tensor* layout, int K,
                  int grad_dtype, const void* const* grads, const float* const* m,
                  lco_diag* out);
 
+/*
+ * The max-norm quantizer with stochastic rounding that the pages compare L1
+ * quantization against ([LC] "Core claim": the standard max-norm quantizer
+ * Q_inf collapses most entries of Lion's heavy-tailed update to zero; Fig. 4
+ * caption: Q_inf stochastic quantization clips most values to zero, giving
+ * low match and flip rates; the referee report: Q_inf uses stochastic
+ * rounding).  The pages do not print it; the reading here:
+ *   M_inf = max |c| over the tensor (per worker), inv = qmax / M_inf in fp32
+ *   (0 when M_inf == 0), y = |c| * inv in fp32, q = floor(y) + (u < y -
+ *   floor(y) ? 1 : 0), clamped to qmax, with the sign of c; qmax = 2^(n-1)-1.
+ * u is uniform in [0, 1): the top 24 bits of one SplitMix64 output times
+ * 2^-24 (lco_qinf_uniform).
+ */
+
+/* SplitMix64 (Steele, Lea and Flood 2014): output number k (k = 0, 1, ...)
+ * of the generator whose state starts at `seed` (state += 0x9e3779b97f4a7c15
+ * before each output, which is the state passed through the mixing
+ * function). */
+uint64_t lco_splitmix64(uint64_t seed, uint64_t k);
+
+/* The uniform of element e (index in the flat parameter vector, < 2^40) of
+ * worker `worker` (< 256) at step t: SplitMix64 output number
+ * (t mod 2^16) * 2^48 + worker * 2^40 + e from `seed`, top 24 bits * 2^-24. */
+float lco_qinf_uniform(uint64_t seed, int64_t t, int worker, int64_t e);
+
+/* max |c[e]| over [0, n); 0 for n == 0. */
+float lco_maxabs(const float* c, int64_t n);
+
+/* Q_inf codes of c[0..n) for worker `worker` at step t; c[e] is element
+ * e_first + e of the flat vector. */
+void lco_qinf(const float* c, int64_t n, int nbits, float maxabs, uint64_t seed, int64_t t, int worker,
+              int64_t e_first, int8_t* q);
+
+/* Per-tensor comparison of the Q_inf aggregate with the full-precision
+ * update: every worker's Q_inf codes (nbits, its own M_inf per tensor) are
+ * summed in worker order; u_q = sign of lco_direction(sum, W, flags without
+ * the average, t); u_fp and the categories as in lco_diagnose; zero_codes
+ * counts the (worker, element) codes equal to 0.  e_base is the flat index
+ * of element 0 of the vector passed (tensors start at e_base + offset). */
+typedef struct {
+    int64_t match, flip, dropped, spurious, zero_codes;
+} lco_qinf_diag;
+
+int lco_diagnose_qinf(int64_t d, int W, const lco_tensor* layout, int K, float beta1, int nbits, uint32_t flags,
+                      int64_t t, uint64_t seed, int64_t e_base, int grad_dtype, const void* const* grads,
+                      const float* const* m, lco_qinf_diag* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,21 @@ MUTATIONS = [
      "        return 2;\n    if (u_q == 0.0f)\n        return 1;"),
     ("diagnose_full_sign_skips_worker_0", "s = (i == 0) ? ci : s + ci;", "s = (i == 0) ? 0.0f : s + ci;"),
     ("diagnose_max_std_keeps_first", "if (sd > r.max_std_m)", "if (r.max_std_m == 0.0f)"),
+    # the Q_inf comparator
+    ("splitmix_counter_off_by_one", "uint64_t z = seed + (k + 1u) * 0x9e3779b97f4a7c15ull;",
+     "uint64_t z = seed + k * 0x9e3779b97f4a7c15ull;"),
+    ("splitmix_shift_wrong", "z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;",
+     "z = (z ^ (z >> 28)) * 0x94d049bb133111ebull;"),
+    ("qinf_uniform_low_bits", "uint64_t bits = lco_splitmix64(seed, k) >> 40; /* 24 bits */",
+     "uint64_t bits = lco_splitmix64(seed, k) & 0xffffffu; /* 24 bits */"),
+    ("qinf_uniform_ignores_worker", "((uint64_t)(unsigned)worker << 40)", "((uint64_t)(unsigned)0 << 40)"),
+    ("qinf_deterministic_floor", "int v = (int)fl + (u < frac ? 1 : 0);", "int v = (int)fl;"),
+    ("qinf_round_up_when_draw_exceeds", "int v = (int)fl + (u < frac ? 1 : 0);", "int v = (int)fl + (u > frac ? 1 : 0);"),
+    ("qinf_scale_by_first_element", "if (fabsf(c[e]) > mx)\n            mx = fabsf(c[e]);",
+     "if (e == 0)\n            mx = fabsf(c[e]);"),
+    ("qinf_sign_dropped", "q[e] = (int8_t)(c[e] < 0.0f ? -v : v);", "q[e] = (int8_t)v;"),
+    ("qinf_local_element_index", "lco_qinf(c, n, nbits, lco_maxabs(c, n), seed, t, i, e_base + off,",
+     "lco_qinf(c, n, nbits, lco_maxabs(c, n), seed, t, i, off,"),
 ]
 
 

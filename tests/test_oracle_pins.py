@@ -542,3 +542,126 @@ def test_diagnose_tie_rate_statistics(oracle_lib):
         assert abs(r["ties"] / d - p) < 5 * math.sqrt(p * (1 - p) / d)
         assert r["dropped"] == r["ties"]  # a tie is never a full-precision zero here
         assert r["match"] > r["flip"]     # the majority usually agrees with the sum
+
+
+# ---------------------------------------------------------------------------
+# Q_inf: max-norm scaling with stochastic rounding, the comparator of the
+# diagnostics ("Lion Cub" page, "Core claim" and the Fig. 4 caption: Q_inf
+# collapses most entries of the heavy-tailed update to zero)
+# ---------------------------------------------------------------------------
+
+def test_splitmix64_published_outputs(oracle_lib):
+    with open(os.path.join(GOLDEN, "splitmix64_vectors.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        want = case.get("outputs") or [int(h, 16) for h in case["outputs_hex"]]
+        got = [oracle.splitmix64(case["seed"], k) for k in range(len(want))]
+        assert got == want, case
+
+
+def test_qinf_uniform_range_and_counter(oracle_lib):
+    us = [oracle.qinf_uniform(5, 3, 2, e) for e in range(4000)]
+    assert all(0.0 <= u < 1.0 for u in us)
+    assert all(u * 16777216.0 == int(u * 16777216.0) for u in us)  # 24-bit grid
+    assert abs(np.mean(us) - 0.5) < 5 * math.sqrt(1 / 12 / len(us))
+    # step, worker and element each select another output of the generator
+    base = oracle.qinf_uniform(5, 3, 2, 7)
+    assert oracle.qinf_uniform(5, 3, 2, 7) == base
+    assert len({base, oracle.qinf_uniform(5, 4, 2, 7), oracle.qinf_uniform(5, 3, 1, 7),
+                oracle.qinf_uniform(5, 3, 2, 8), oracle.qinf_uniform(6, 3, 2, 7)}) == 5
+    # the counter: (t mod 2^16) * 2^48 + worker * 2^40 + e, top 24 bits of the output
+    k = (3 << 48) | (2 << 40) | 7
+    assert base == (oracle.splitmix64(5, k) >> 40) / 16777216.0
+    assert oracle.qinf_uniform(5, 3 + 65536, 2, 7) == base
+
+
+def test_qinf_deterministic_cases(oracle_lib):
+    # power-of-two max-norm: the scale qmax / M_inf is exact, so whole-number
+    # y = qmax |c| / M_inf are exact and rounding has nothing to decide
+    c = np.array([4.0, -4.0, 2.0, -1.0, 0.0, -0.0], np.float32)
+    for seed in (0, 1, 99):
+        q = oracle.qinf(c, 2, seed=seed, t=0, worker=0)        # qmax = 1, y = [1, 1, .5, .25, 0, 0]
+        assert q[0] == 1 and q[1] == -1 and q[4] == 0 and q[5] == 0
+        assert q[2] in (0, 1) and q[3] in (0, -1)
+        q8 = oracle.qinf(np.array([8.0, -6.0, 2.0, 0.0], np.float32), 4, seed=seed, t=1, worker=3)  # inv = 7/8
+        assert list(q8[[0, 3]]) == [7, 0] and q8[1] in (-5, -6) and q8[2] in (1, 2)
+    # every |c| equal: each code is +-qmax whatever the draw
+    c = np.where(np.arange(1000) % 3 == 0, -0.25, 0.25).astype(np.float32)
+    for n in (2, 4, 8):
+        q = oracle.qinf(c, n, seed=7, t=2, worker=1)
+        qmax = (1 << (n - 1)) - 1
+        assert np.array_equal(q, np.where(c < 0, -qmax, qmax))
+    # an all-zero tensor (M_inf = 0) gives zero codes
+    assert not oracle.qinf(np.zeros(64, np.float32), 4, seed=1, t=0, worker=0).any()
+    assert oracle.maxabs(np.array([0.5, -3.0, 2.0], np.float32)) == 3.0
+
+
+def test_qinf_is_unbiased_stochastic_rounding(oracle_lib):
+    # 200,000 copies of 0.3 next to one 1.0: y = RN(0.3 * 7) = 2.1 (n = 4);
+    # codes are 2 or 3, and their mean is y within the binomial error (a
+    # floor, a round-to-nearest or a draw compared the wrong way fails)
+    n = 200_001
+    c = np.full(n, 0.3, np.float32)
+    c[0] = 1.0
+    q = oracle.qinf(c, 4, seed=11, t=0, worker=0)[1:].astype(np.float64)
+    y = float(np.float32(np.float32(0.3) * np.float32(7.0)))
+    frac = y - math.floor(y)
+    assert set(np.unique(q)) <= {2.0, 3.0}
+    assert abs(q.mean() - y) < 5 * math.sqrt(frac * (1 - frac) / q.size)
+    # negative values mirror
+    qn = oracle.qinf(-c, 4, seed=11, t=0, worker=0)[1:].astype(np.float64)
+    assert abs(qn.mean() + y) < 5 * math.sqrt(frac * (1 - frac) / q.size)
+
+
+def test_qinf_collapses_heavy_tails_where_q1_does_not(oracle_lib):
+    # the pages' observation, on Student-t(3) values: most Q_inf codes are 0,
+    # while most Eq. (1) codes are not
+    rng = np.random.default_rng(3)
+    x = (rng.standard_t(3.0, size=1 << 18) * 1e-3).astype(np.float32)
+    for n in (2, 4):
+        zq = np.mean(oracle.qinf(x, n, seed=2, t=0, worker=0) == 0)
+        z1 = np.mean(oracle.q1(x, n) == 0)
+        assert zq > 0.8 and z1 < zq, (n, zq, z1)
+    assert np.mean(oracle.q1(x, 4) == 0) < 0.5
+
+
+def test_diagnose_qinf_hand_case(oracle_lib):
+    # beta1 = 0 so c = g; two workers, one tensor of 4 elements, n = 2
+    # worker 0: [4, -4, 2, 0] (M_inf 4: codes 1, -1, 0 or 1, 0)
+    # worker 1: [1, -1, -1, 0] (M_inf 1: codes 1, -1, -1, 0)
+    g0 = np.array([4, -4, 2, 0], np.float32)
+    g1 = np.array([1, -1, -1, 0], np.float32)
+    m = [np.zeros(4, np.float32), np.zeros(4, np.float32)]
+    for seed in range(8):
+        r = oracle.diagnose_qinf(d=4, W=2, layout=None, beta1=0.0, nbits=2, flags=0, t=0, seed=seed, e_base=0,
+                                 grads=[g0, g1], m=m)[0]
+        q02 = oracle.qinf(g0, 2, seed=seed, t=0, worker=0)[2]
+        # e0: 1 + 1 = 2, s = 5 -> match; e1: -2, s = -5 -> match; e3: 0, s = 0 -> match
+        # e2: q02 - 1 (0 or -1) against s = 1 -> dropped or flip
+        want = {"match": 3, "flip": 1 if q02 == 0 else 0, "dropped": 1 if q02 == 1 else 0, "spurious": 0}
+        assert {f: r[f] for f in want} == want, (seed, r)
+        assert r["zero_codes"] == 2 + (1 if q02 == 0 else 0)
+    # the element index is global: the same tensor at another flat offset draws other numbers
+    r_off = [oracle.diagnose_qinf(d=4, W=2, layout=None, beta1=0.0, nbits=2, flags=0, t=0, seed=s, e_base=1 << 20,
+                                  grads=[g0, g1], m=m)[0]["flip"] for s in range(32)]
+    r_0 = [oracle.diagnose_qinf(d=4, W=2, layout=None, beta1=0.0, nbits=2, flags=0, t=0, seed=s, e_base=0,
+                                grads=[g0, g1], m=m)[0]["flip"] for s in range(32)]
+    assert r_off != r_0
+
+
+def test_diagnose_qinf_partitions_each_tensor(oracle_lib):
+    rng = np.random.default_rng(4)
+    d, W = 3000, 4
+    layout = [(0, 1000, 0), (1000, 1968, 0), (2968, 32, 0)]
+    grads = [(rng.standard_t(3.0, d) * 1e-3).astype(np.float32) for _ in range(W)]
+    m = [(rng.standard_normal(d) * 1e-4).astype(np.float32) for _ in range(W)]
+    recs = oracle.diagnose_qinf(d=d, W=W, layout=layout, beta1=0.9, nbits=4, flags=0, t=5, seed=9, e_base=0,
+                                grads=grads, m=m)
+    for (off, n, _), r in zip(layout, recs):
+        assert r["match"] + r["flip"] + r["dropped"] + r["spurious"] == n
+        assert 0 <= r["zero_codes"] <= W * n
+        # a tensor on its own, given its flat offset, gives the same record
+        one = oracle.diagnose_qinf(d=n, W=W, layout=None, beta1=0.9, nbits=4, flags=0, t=5, seed=9, e_base=off,
+                                   grads=[g[off:off + n].copy() for g in grads],
+                                   m=[x[off:off + n].copy() for x in m])[0]
+        assert one == r
