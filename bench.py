@@ -584,9 +584,28 @@ def run_diagnose(args, wl, h, dev, stream, grad_ptrs):
     G = 4 if wl.grad == "f32" else 2
     alg = wl.d * wl.W * (G + 4) * (2 if wl.mode == 1 else 1)  # (+ the M1 pass in L1 mode)
     worst = max(range(K), key=lambda k: recs[k]["max_std_m"])
+    # the max-norm comparator (stochastic rounding) at the workload's code
+    # width, 4 bits for sign-mode workloads
+    qbits = wl.nbits if wl.mode == 1 else 4
+    qout = torch.zeros(K * lc.QINF_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        lc.lioncub_diagnose_qinf(h, grad_ptrs, qbits, 0, qout.data_ptr(), sp)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        lc.lioncub_diagnose_qinf(h, grad_ptrs, qbits, 0, qout.data_ptr(), sp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    qms = e0.elapsed_time(e1) / n
+    qrecs = lc.decode_qinf(qout.cpu().numpy().tobytes(), K)
+    qtot = {f: sum(r[f] for r in qrecs) for f in lc.QINF_FIELDS}
+    qalg = 2 * wl.d * wl.W * (G + 4)  # the max-norm pass and the counting pass
     return {"ms": ms, "alg_bytes": alg, "gbs": alg / (ms * 1e-3) / 1e9,
             "fractions": {f: v / wl.d for f, v in tot.items()},
             "max_std_m": {"tensor": wl.layout[worst][0], "value": recs[worst]["max_std_m"]},
+            "qinf": {"nbits": qbits, "ms": qms, "alg_bytes": qalg, "gbs": qalg / (qms * 1e-3) / 1e9,
+                     "fractions": {f: qtot[f] / wl.d for f in ("match", "flip", "dropped", "spurious")},
+                     "zero_code_fraction": qtot["zero_codes"] / (wl.d * wl.W)},
             "state": "after the warm-up and timed steps"}
 
 

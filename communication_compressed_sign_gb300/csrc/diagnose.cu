@@ -174,6 +174,152 @@ __global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub
     }
 }
 
+// ---- the Q_inf comparator (lioncub_diagnose_qinf) ----------------------------
+//
+// The max-norm quantizer with stochastic rounding that the pages compare L1
+// quantization against ("Lion Cub" page, "Core claim" and the Fig. 4
+// caption: it collapses most entries of the heavy-tailed update to zero).
+// Per (worker, tensor): M_inf = max |c|; inv = RN(qmax / M_inf) (0 when
+// M_inf == 0); per element y = RN(|c| * inv), code = floor(y) + (u < y -
+// floor(y)), clamped to qmax, with the sign of c.  u is the top 24 bits of
+// SplitMix64 (Steele, Lea and Flood 2014) output number (t mod 2^16) * 2^48 +
+// worker * 2^40 + e from the caller's seed, times 2^-24.  The codes are
+// summed over the workers in order and the sign of the sum (ties by the
+// handle's tie rule) is compared with the full-precision sign.
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t k)
+{
+    uint64_t z = seed + (k + 1ull) * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+// max |c| of each (worker, tensor): one block per (tile, worker), an integer
+// atomicMax on the bits of the non-negative float (exact, order-free)
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) k_qinf_maxabs(const StepArgs a, float* maxabs)
+{
+    __shared__ float red[kThreads / 32];
+    const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
+    const int i = blockIdx.y;
+    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
+        valid = 0;
+    int k = static_cast<int>(tl.meta & ~kTileSync);
+    if (!in_bounds(a, k < a.K))
+        k = 0;
+    float mx = 0.0f;
+    if (valid > 0) {
+        float g[kVec], m[kVec];
+        load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+            if (j < valid)
+                mx = fmaxf(mx, fabsf(update_vector(m[j], g[j], a.beta1, a.omega1)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.0f;
+        for (int w = 0; w < kThreads / 32; ++w)
+            b = fmaxf(b, red[w]);
+        if (b > 0.0f)
+            atomicMax(reinterpret_cast<int*>(maxabs + static_cast<int64_t>(i) * a.K + k), __float_as_int(b));
+    }
+}
+
+template <typename GT, int NB>
+__global__ void __launch_bounds__(kThreads) k_diagnose_qinf(const StepArgs a, const float* maxabs, uint64_t seed,
+                                                            lioncub_qinf_diag* out)
+{
+    __shared__ unsigned long long red[kThreads / 32][5];
+    const Tile tl = in_bounds(a, blockIdx.x < a.ntiles) ? a.tiles[blockIdx.x] : Tile{0, 0, 0u};
+    const int64_t e0 = tl.start + static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t left = tl.start + tl.len - e0;
+    int valid = left <= 0 ? 0 : (left >= kVec ? kVec : static_cast<int>(left));
+    if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
+        valid = 0;
+    int k = static_cast<int>(tl.meta & ~kTileSync);
+    if (!in_bounds(a, k < a.K))
+        k = 0;
+    constexpr int kQmax = (1 << (NB - 1)) - 1;
+    int agg[kVec];
+    float s[kVec];
+    uint32_t zeros = 0;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        agg[j] = 0;
+        s[j] = 0.0f;
+    }
+    if (valid > 0) {
+        for (int i = 0; i < a.W; ++i) {
+            float g[kVec], m[kVec];
+            load_gm<GT>(a.g[i], a.m[i], e0, valid, g, m);
+            const float mi = maxabs[static_cast<int64_t>(i) * a.K + k];
+            const float inv = mi > 0.0f ? __fdiv_rn(static_cast<float>(kQmax), mi) : 0.0f;
+            const uint64_t kbase = (static_cast<uint64_t>(a.qinf_step & 0xffff) << 48) |
+                                   (static_cast<uint64_t>(i) << 40) | static_cast<uint64_t>(e0);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float c = update_vector(m[j], g[j], a.beta1, a.omega1);
+                const float y = __fmul_rn(fabsf(c), inv);
+                const float fl = floorf(y);
+                const float frac = __fsub_rn(y, fl);
+                const float u = static_cast<float>(static_cast<uint32_t>(splitmix64(seed, kbase + j) >> 40)) *
+                                (1.0f / 16777216.0f);
+                int v = static_cast<int>(fl) + (u < frac ? 1 : 0);
+                v = min(v, kQmax);
+                const int q = c < 0.0f ? -v : v;
+                if (j < valid) {
+                    agg[j] += q;
+                    zeros += (q == 0) ? 1u : 0u;
+                }
+                s[j] = (i == 0) ? c : __fadd_rn(s[j], c);
+            }
+        }
+    }
+    uint32_t cnt[5] = {0, 0, 0, 0, zeros};  // match, flip, dropped, spurious, zero codes
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        if (j < valid) {
+            const float uq = agg[j] > 0 ? 1.0f : (agg[j] < 0 ? -1.0f : a.tie_u);
+            const float uf = sgn(s[j]);
+            if (uq == uf)
+                cnt[0] += 1;
+            else if (uq != 0.0f && uf != 0.0f)
+                cnt[1] += 1;
+            else if (uq == 0.0f)
+                cnt[2] += 1;
+            else
+                cnt[3] += 1;
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 5; ++c)
+        cnt[c] = warp_sum(cnt[c]);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 5; ++c)
+            red[warp][c] = cnt[c];
+    }
+    __syncthreads();
+    if (threadIdx.x < 5) {
+        unsigned long long tot = 0;
+        for (int w = 0; w < kThreads / 32; ++w)
+            tot += red[w][threadIdx.x];
+        if (tot)
+            atomicAdd(reinterpret_cast<unsigned long long*>(&out[k]) + threadIdx.x, tot);
+    }
+}
+
 template <typename GT>
 cudaError_t launch_typed(const StepArgs& a, int nb, lioncub_diag* out, cudaStream_t s)
 {
@@ -198,6 +344,41 @@ cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lion
     if (grad_dtype == LIONCUB_GRAD_BF16)
         return launch_typed<__nv_bfloat16>(a, nb, out, s);
     return launch_typed<float>(a, nb, out, s);
+}
+
+}  // namespace lc
+
+namespace lc {
+namespace {
+
+template <typename GT>
+cudaError_t launch_qinf_typed(const StepArgs& a, int nbits, float* maxabs, uint64_t seed, lioncub_qinf_diag* out,
+                              cudaStream_t s)
+{
+    k_qinf_maxabs<GT><<<dim3(static_cast<unsigned>(a.ntiles), a.W), kThreads, 0, s>>>(a, maxabs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const unsigned grid = static_cast<unsigned>(a.ntiles);
+    switch (nbits) {
+    case 2: k_diagnose_qinf<GT, 2><<<grid, kThreads, 0, s>>>(a, maxabs, seed, out); break;
+    case 4: k_diagnose_qinf<GT, 4><<<grid, kThreads, 0, s>>>(a, maxabs, seed, out); break;
+    case 8: k_diagnose_qinf<GT, 8><<<grid, kThreads, 0, s>>>(a, maxabs, seed, out); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_diagnose_qinf(const StepArgs& a, int grad_dtype, int nbits, float* maxabs, uint64_t seed,
+                                 lioncub_qinf_diag* out, cudaStream_t s)
+{
+    if (a.ntiles == 0)
+        return cudaSuccess;
+    if (grad_dtype == LIONCUB_GRAD_BF16)
+        return launch_qinf_typed<__nv_bfloat16>(a, nbits, maxabs, seed, out, s);
+    return launch_qinf_typed<float>(a, nbits, maxabs, seed, out, s);
 }
 
 }  // namespace lc

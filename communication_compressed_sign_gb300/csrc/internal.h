@@ -56,6 +56,7 @@ struct StepArgs {
     float* sync_buf;      // new momenta of synchronized tiles, worker-major, sync_slots each:
                           // written by the compress pass, read (all ranks' workers) by the apply
     int64_t sync_slots;   // elements per worker in the sync buffers (synchronized tiles x 2048)
+    int64_t qinf_step;    // the step index t (lioncub_diagnose_qinf's random counters)
     int W;
     int K;
     int nbits;
@@ -99,6 +100,8 @@ cudaError_t launch_m1_finalize(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_reduce_apply(const StepArgs& a, int l1_mode, cudaStream_t s);
 cudaError_t launch_export_agg(const StepArgs& a, int l1_mode, int32_t* agg, cudaStream_t s);
 cudaError_t launch_diagnose(const StepArgs& a, int grad_dtype, int l1_mode, lioncub_diag* out, cudaStream_t s);
+cudaError_t launch_diagnose_qinf(const StepArgs& a, int grad_dtype, int nbits, float* maxabs, uint64_t seed,
+                                 lioncub_qinf_diag* out, cudaStream_t s);
 
 // data-parallel exchange (dist.cu)
 cudaError_t launch_compress_dist(const StepArgs& a, int grad_dtype, int l1_mode, cudaStream_t s);

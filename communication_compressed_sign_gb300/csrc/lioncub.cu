@@ -25,6 +25,7 @@ using lc::Tile;
 // Layouts the language bindings rely on.
 static_assert(sizeof(lioncub_tensor) == 24, "lioncub_tensor must stay 24 bytes");
 static_assert(sizeof(lioncub_diag) == 48, "lioncub_diag must stay 48 bytes");
+static_assert(sizeof(lioncub_qinf_diag) == 40, "lioncub_qinf_diag must stay 40 bytes");
 static_assert(sizeof(lioncub_dist_plan) == 104, "lioncub_dist_plan must stay 104 bytes");
 static_assert(sizeof(StepArgs) <= 4096, "kernel parameters must fit the classic 4 KB limit");
 static_assert(lc::kStatusWaitTimeout == LIONCUB_STATUS_WAIT_TIMEOUT &&
@@ -65,6 +66,7 @@ struct lioncub_s {
     float* m1 = nullptr;
     float* inv = nullptr;
     int* status = nullptr;  // set by a kernel whose bounded wait gave up
+    float* maxabs = nullptr;  // W x K max |c| of lioncub_diagnose_qinf (allocated on its first call)
     // lioncub_step_host: double-buffered staging, an upload stream and the
     // events that order uploads against the steps that read them
     void* staging[2] = {nullptr, nullptr};
@@ -165,6 +167,7 @@ void free_scratch(lioncub_t h)
     h->partials = nullptr;
     h->m1 = h->inv = nullptr;
     h->status = nullptr;
+    h->maxabs = nullptr;
     h->staging[0] = h->staging[1] = nullptr;
     h->nstaging = 0;
     for (int b = 0; b < 2; ++b) {
@@ -1044,6 +1047,49 @@ int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_diag* out_de
     prof_end(h, slot, s);
     if (e != cudaSuccess)
         return cuda_fail(h, e, "diagnose launch");
+    return LIONCUB_OK;
+}
+
+int lioncub_diagnose_qinf(lioncub_t h, const void* const* grads, int nbits, uint64_t seed, lioncub_qinf_diag* out_dev,
+                          lioncub_stream_t stream)
+{
+    if (!h)
+        return LIONCUB_ERR_ARG;
+    if (h->dist)
+        return fail(h, LIONCUB_ERR_STATE, "diagnostics need every worker on one GPU (not a data-parallel handle)");
+    if (!h->bound)
+        return fail(h, LIONCUB_ERR_STATE, "lioncub_bind_state has not been called");
+    if (!grads || !out_dev)
+        return fail(h, LIONCUB_ERR_ARG, "grads and out_dev must be non-NULL");
+    if (nbits != 2 && nbits != 4 && nbits != 8)
+        return fail(h, LIONCUB_ERR_ARG, "nbits must be 2, 4 or 8 (got %d)", nbits);
+    if (reinterpret_cast<uintptr_t>(out_dev) & 7u)
+        return fail(h, LIONCUB_ERR_ALIGN, "out_dev is not 8-byte aligned");
+    for (int i = 0; i < h->W; ++i) {
+        if (!grads[i])
+            return fail(h, LIONCUB_ERR_ARG, "grads[%d] is NULL", i);
+        if (!aligned16(grads[i]))
+            return fail(h, LIONCUB_ERR_ALIGN, "grads[%d] is not 16-byte aligned", i);
+    }
+    if (!h->maxabs) {
+        const cudaError_t e = dev_alloc(h, &h->maxabs, static_cast<size_t>(h->W) * h->K);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, e == cudaErrorMemoryAllocation ? LIONCUB_ERR_OOM : LIONCUB_ERR_CUDA,
+                        "Q_inf scratch allocation failed");
+        }
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NvtxRange range("lioncub_diagnose_qinf");
+    StepArgs a = make_args(h, grads);
+    a.qinf_step = h->t;
+    cudaError_t e = cudaMemsetAsync(out_dev, 0, static_cast<size_t>(h->K) * sizeof(lioncub_qinf_diag), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(h->maxabs, 0, static_cast<size_t>(h->W) * h->K * sizeof(float), s);
+    if (e == cudaSuccess)
+        e = lc::launch_diagnose_qinf(a, h->grad_dtype, nbits, h->maxabs, seed, out_dev, s);
+    if (e != cudaSuccess)
+        return cuda_fail(h, e, "Q_inf diagnostics");
     return LIONCUB_OK;
 }
 

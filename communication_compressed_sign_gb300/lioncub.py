@@ -38,6 +38,8 @@ KERNEL_NAMES = {KERNEL_COMPRESS: "compress", KERNEL_M1: "m1_partial",
                 KERNEL_DIAGNOSE: "diagnose"}
 DIAG_FIELDS = ("match", "flip", "dropped", "spurious", "ties", "max_std_m")
 DIAG_BYTES = 48
+QINF_FIELDS = ("match", "flip", "dropped", "spurious", "zero_codes")
+QINF_BYTES = 40
 
 # Every symbol the header declares, for load checks.
 EXPORTED = (
@@ -47,7 +49,7 @@ EXPORTED = (
     "lioncub_last_error", "lioncub_strerror", "lioncub_destroy", "lioncub_sign_step_noalloc",
     "lioncub_diagnose", "lioncub_host_alloc", "lioncub_host_free",
     "lioncub_dist_plan_make", "lioncub_dist_create", "lioncub_dist_bind_buffers", "lioncub_dist_compress",
-    "lioncub_dist_reduce", "lioncub_dist_apply",
+    "lioncub_dist_reduce", "lioncub_dist_apply", "lioncub_diagnose_qinf",
 )
 # exchange buffers of the data-parallel step (LIONCUB_DIST_*)
 DIST_SEND, DIST_RECV, DIST_DIR_CHUNK, DIST_DIR_ALL, DIST_AGG, DIST_SYNC_SEND, DIST_SYNC_RECV = range(7)
@@ -112,6 +114,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.lioncub_sign_step_noalloc.restype = i32
         L.lioncub_diagnose.argtypes = [vp, vp, vp, vp]
         L.lioncub_diagnose.restype = i32
+        L.lioncub_diagnose_qinf.argtypes = [vp, vp, i32, ctypes.c_uint64, vp, vp]
+        L.lioncub_diagnose_qinf.restype = i32
         L.lioncub_host_alloc.argtypes = [ctypes.POINTER(vp), ctypes.c_size_t]
         L.lioncub_host_alloc.restype = i32
         L.lioncub_host_free.argtypes = [vp]
@@ -242,6 +246,18 @@ def lioncub_debug_export(h: int, what: int, dst_ptr: int, stream: int = 0) -> No
 def lioncub_diagnose(h: int, grad_ptrs, out_ptr: int, stream: int = 0) -> None:
     """Fill K lioncub_diag records (48 bytes each) at device address out_ptr."""
     _check(load().lioncub_diagnose(h, ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), out_ptr, stream or None), h)
+
+
+def lioncub_diagnose_qinf(h: int, grad_ptrs, nbits: int, seed: int, out_ptr: int, stream: int = 0) -> None:
+    """Fill K lioncub_qinf_diag records (40 bytes each) at device address out_ptr."""
+    _check(load().lioncub_diagnose_qinf(h, ctypes.cast(_ptrs(grad_ptrs), ctypes.c_void_p), nbits,
+                                        seed & (2**64 - 1), out_ptr, stream or None), h)
+
+
+def decode_qinf(raw: bytes, K: int):
+    """Host bytes of K lioncub_qinf_diag records -> list of dicts."""
+    import struct
+    return [dict(zip(QINF_FIELDS, struct.unpack_from("<5q", raw, k * QINF_BYTES))) for k in range(K)]
 
 
 def decode_diag(raw: bytes, K: int):

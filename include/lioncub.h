@@ -300,6 +300,35 @@ LIONCUB_API int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_
                                  lioncub_stream_t stream);
 
 /*
+ * The max-norm quantizer the pages compare Eq. (1) against, as a comparator
+ * of the same kind: [LC] "Core claim" (the standard max-norm quantizer Q_inf
+ * collapses most entries of Lion's heavy-tailed update to zero), the Fig. 4
+ * caption (Q_inf stochastic quantization clips most values to zero, giving
+ * low match and flip rates) and the referee report (Q_inf rounds
+ * stochastically).  The pages do not print Q_inf; this library reads it as:
+ * per (worker, tensor) M_inf = max |c|, inv = RN(qmax / M_inf) (0 when
+ * M_inf == 0), y = RN(|c| * inv), code = floor(y) + (u < y - floor(y) ? 1 :
+ * 0), clamped to qmax = 2^(nbits-1) - 1, with the sign of c; u is the top 24
+ * bits of SplitMix64 (Steele, Lea and Flood 2014) output number
+ * (t mod 2^16) * 2^48 + i * 2^40 + e of the generator started from `seed`,
+ * times 2^-24 (t the handle's step counter, i the worker, e the element's
+ * flat index).  The codes of the W workers are summed in order, and the
+ * sign of the sum (ties by the handle's tie rule; never the average) is
+ * compared, per element, with the sign of the full-precision sum of c as in
+ * lioncub_diagnose.  Nothing is updated.  out_dev: K records in device memory
+ * the caller owns, 8-byte aligned, zeroed and filled on `stream`.  nbits: 2,
+ * 4 or 8, whatever the handle's mode.  Errors: ERR_STATE (unbound, or a
+ * data-parallel handle), ERR_ARG, ERR_ALIGN, ERR_OOM (its W x K scratch is
+ * allocated on the first call), ERR_CUDA.
+ */
+typedef struct {
+    int64_t match, flip, dropped, spurious;
+    int64_t zero_codes; /* (worker, element) codes equal to 0 */
+} lioncub_qinf_diag;
+LIONCUB_API int lioncub_diagnose_qinf(lioncub_t h, const void* const* grads, int nbits, uint64_t seed,
+                                      lioncub_qinf_diag* out_dev, lioncub_stream_t stream);
+
+/*
  * Per-kernel timing with CUDA events on the step's stream.  lioncub_profile
  * (h, n) records an event pair around every kernel launch of the next n
  * lioncub_step calls (and of lioncub_diagnose calls made while steps remain

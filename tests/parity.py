@@ -325,3 +325,60 @@ def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_
         return res
     finally:
         lc.lioncub_destroy(h)
+
+
+def run_qinf_parity(wl: synth.Workload, tensor_names, nbits: int, seed: int, warm_steps: int = 2,
+                    mode_flags: int = 0):
+    """Warm the state up with `warm_steps` GPU steps, then compare
+    lioncub_diagnose_qinf for the next step's gradients with the oracle's
+    Q_inf comparison on the named whole tensors (every field exact; the
+    random counters use each tensor's flat offset).  Returns the GPU records
+    of those tensors."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    W, d = wl.W, wl.d
+    gdt = synth.grad_dtype(wl)
+    theta = torch.empty(d, dtype=torch.float32, device=dev)
+    synth.fill_theta_(theta, wl)
+    m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+    grads = [torch.empty(d, dtype=gdt, device=dev) for _ in range(W)]
+    mode_flags |= wl.flags
+    h = lc.lioncub_create(d, W, synth.abi_layout(wl.layout), wl.beta1, wl.beta2, wl.lr, wl.wd,
+                          wl.mode | mode_flags, wl.nbits, lc.GRAD_F32 if wl.grad == "f32" else lc.GRAD_BF16,
+                          wl.sync_interval)
+    try:
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        s = torch.cuda.current_stream().cuda_stream
+        for t in range(warm_steps):
+            for i in range(W):
+                synth.fill_grad_(grads[i], wl, t, i)
+            lc.lioncub_step(h, [g.data_ptr() for g in grads], s)
+        t = warm_steps
+        for i in range(W):
+            synth.fill_grad_(grads[i], wl, t, i)
+        K = len(wl.layout)
+        out = torch.full((K * lc.QINF_BYTES,), 0xAB, dtype=torch.uint8, device=dev)
+        theta_before = theta.clone()
+        lc.lioncub_diagnose_qinf(h, [g.data_ptr() for g in grads], nbits, seed, out.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert lc.lioncub_get_step(h) == t and torch.equal(theta, theta_before)  # nothing updated
+        gpu = lc.decode_qinf(out.cpu().numpy().tobytes(), K)
+        res = []
+        for k, (name, off, n, fl) in enumerate(wl.layout):
+            if name not in tensor_names:
+                continue
+            g_o = []
+            for i in range(W):
+                gi = grads[i][off:off + n].cpu()
+                g_o.append(gi.view(torch.int16).numpy().view(np.uint16).copy() if wl.grad == "bf16"
+                           else gi.numpy().copy())
+            m_o = [x[off:off + n].cpu().numpy().copy() for x in m]
+            o = oracle.diagnose_qinf(d=n, W=W, layout=None, beta1=wl.beta1, nbits=nbits, flags=mode_flags, t=t,
+                                     seed=seed, e_base=off, grads=g_o, m=m_o)[0]
+            assert gpu[k] == o, (name, gpu[k], o)
+            assert sum(gpu[k][f] for f in ("match", "flip", "dropped", "spurious")) == n
+            res.append((name, gpu[k]))
+        return res
+    finally:
+        lc.lioncub_destroy(h)

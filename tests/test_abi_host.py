@@ -34,7 +34,7 @@ def _declared():
 
 def test_header_symbols_exported(lc):
     declared = _declared()
-    assert len(declared) == 24
+    assert len(declared) == 25
     lib = ctypes.CDLL(lc.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name

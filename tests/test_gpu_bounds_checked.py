@@ -26,7 +26,7 @@ def test_parity_cases_under_bounds_checks():
     __graft_entry__.build()
     lib = build.build(bounds_check=True)
     sel = ("small_ragged or multi_tensor or tie_and_average or exact_zero or all_layer or workload1 "
-           "or guard_bands or diagnose_small or host_buffer or empty_vector or many_small")
+           "or guard_bands or diagnose_small or diagnose_qinf_small or host_buffer or empty_vector or many_small")
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_gpu_parity.py", "-m", "gpu", "-x", "-q",
                         "-p", "no:cacheprovider", "-k", sel],
                        cwd=ROOT, env={**os.environ, "LIONCUB_LIBRARY": lib}, capture_output=True, text=True,

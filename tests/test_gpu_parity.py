@@ -427,6 +427,31 @@ def test_diagnose_full_size_workloads():
             print(key, name, r)
 
 
+@pytest.mark.parametrize("mode,nbits,flags,qbits", [(0, 1, 0, 2), (0, 1, lc.FLAG_TIE_ALTERNATE, 4), (1, 4, 0, 4),
+                                                      (1, 2, 0, 8), (0, 1, lc.FLAG_AVERAGE, 4)])
+def test_diagnose_qinf_small(mode, nbits, flags, qbits):
+    """The Q_inf comparator ("Lion Cub" page, "Core claim" and Fig. 4 caption)
+    against the oracle on every tensor of a ragged multi-tensor layout:
+    every count exact, with each code width and tie rule."""
+    layout = _multi_layout(sync=False)
+    wl = _small(synth.layout_total(layout), 6, "bf16", mode, nbits, layout=layout)
+    parity.run_qinf_parity(wl, {n for (n, _, _, _) in layout}, qbits, seed=12345, warm_steps=3, mode_flags=flags)
+
+
+def test_diagnose_qinf_full_size_workloads():
+    """Q_inf at full size: GPT-2 small (W = 8) and the 1.3B layout (n = 2 as
+    its codes), sampled tensors checked whole; most Q_inf codes are zero on
+    the heavy-tailed update (the pages' observation)."""
+    for key, names, qbits in ((2, {"wpe", "h5.mlp.c_fc.b", "h7.attn.c_proj.w", "ln_f.w"}, 4),
+                              (5, {"wpe", "h3.ln_1.b", "h9.attn.c_proj.w", "ln_f.b"}, 2)):
+        res = parity.run_qinf_parity(WL[key], names, qbits, seed=7, warm_steps=2)
+        for name, r in res:
+            n = [x for x in WL[key].layout if x[0] == name][0][2]
+            if n >= 500_000:  # a large tensor's max-norm sits far out in the tail
+                assert r["zero_codes"] > 0.5 * WL[key].W * n, (key, name, r)
+            print(key, name, r)
+
+
 # ---------------------------------------------------------------------------
 # beyond 32-bit element indices
 # ---------------------------------------------------------------------------
