@@ -48,10 +48,11 @@ __global__ void __launch_bounds__(kThreads, 8) k_compress_dist(const StepArgs a)
     if (valid > 0 && !in_bounds(a, e0 >= 0 && e0 + valid <= a.d))
         valid = 0;
 
-    // wire row and the element's position in it
+    // wire row and the element's position in it (sign mode is chunk-major,
+    // L1 mode has one row per worker)
     uint32_t* row;
     int64_t er;
-    if (a.chunk > 0) {
+    if constexpr (NB == 1) {
         // chunk is a multiple of 4096 and a 32-element word never spans two chunks
         const int64_t c = static_cast<int64_t>(static_cast<uint32_t>(e0 >> 12) /
                                                static_cast<uint32_t>(a.chunk >> 12));

@@ -831,7 +831,7 @@ int lioncub_dist_compress(lioncub_t h, const void* const* grads, lioncub_stream_
     const bool l1 = h->mode == LIONCUB_MODE_L1_INTSUM;
     StepArgs a = dist_args(h, grads);
     a.sync_buf = static_cast<float*>(h->xbuf[LIONCUB_DIST_SYNC_SEND]);
-    if (!l1) {
+    if (!l1) {  // (the compress pass writes signs chunk-major: the plan's chunk is a multiple of 4096)
         a.wire = static_cast<uint32_t*>(h->xbuf[LIONCUB_DIST_SEND]);
         a.wire_stride = 0;
         a.chunk = h->plan.chunk;

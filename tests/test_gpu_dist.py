@@ -218,3 +218,67 @@ def test_nccl_single_rank_group(lc, mode, nbits, sync):
             opt.close()
     finally:
         dist.destroy_process_group()
+
+
+def test_exchange_call_order_and_handles(lc):
+    """The three exchange calls run in order only (ERR_STATE otherwise, the
+    step counter unchanged), need their buffers bound, and a data-parallel
+    handle refuses the single-GPU step, host step and diagnostics."""
+    from communication_compressed_sign_gb300 import dist as cdist
+
+    dev = torch.device("cuda", 0)
+    d, W, N = 10_000, 4, 2
+    h = lc.lioncub_dist_create(d, W, N, 1, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
+    try:
+        theta = torch.zeros(d, dtype=torch.float32, device=dev)
+        m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W // N)]
+        g = [torch.zeros(d, dtype=torch.bfloat16, device=dev) for _ in range(W // N)]
+        lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
+        with pytest.raises(lc.LionCubError) as e:  # buffers not bound yet
+            lc.lioncub_dist_compress(h, [x.data_ptr() for x in g])
+        assert e.value.code == lc.ERR_STATE
+        plan = lc.lioncub_dist_plan_make(d, W, N, 1, None, 0, 1, 0)
+        bufs = cdist.allocate_buffers(plan, dev)
+        ptrs = [b.data_ptr() if b is not None else 0 for b in bufs]
+        missing = list(ptrs)
+        missing[lc.DIST_RECV] = 0
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_dist_bind_buffers(h, missing)
+        assert e.value.code == lc.ERR_ARG
+        misaligned = list(ptrs)
+        misaligned[lc.DIST_SEND] += 4
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_dist_bind_buffers(h, misaligned)
+        assert e.value.code == lc.ERR_ALIGN
+        lc.lioncub_dist_bind_buffers(h, ptrs)
+        for call in (lambda: lc.lioncub_dist_reduce(h), lambda: lc.lioncub_dist_apply(h)):
+            with pytest.raises(lc.LionCubError) as e:
+                call()
+            assert e.value.code == lc.ERR_STATE and "out of order" in str(e.value)
+        lc.lioncub_dist_compress(h, [x.data_ptr() for x in g])
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_dist_compress(h, [x.data_ptr() for x in g])
+        assert e.value.code == lc.ERR_STATE
+        lc.lioncub_dist_reduce(h)
+        assert lc.lioncub_get_step(h) == 0
+        lc.lioncub_dist_apply(h)
+        assert lc.lioncub_get_step(h) == 1
+        torch.cuda.synchronize()
+        host = torch.zeros(d, dtype=torch.float32)
+        for call in (lambda: lc.lioncub_step(h, [x.data_ptr() for x in g]),
+                     lambda: lc.lioncub_step_host(h, [x.data_ptr() for x in g], host.data_ptr()),
+                     lambda: lc.lioncub_diagnose(h, [x.data_ptr() for x in g], theta.data_ptr()),
+                     lambda: lc.lioncub_diagnose_qinf(h, [x.data_ptr() for x in g], 4, 0, theta.data_ptr())):
+            with pytest.raises(lc.LionCubError) as e:
+                call()
+            assert e.value.code == lc.ERR_STATE
+    finally:
+        lc.lioncub_destroy(h)
+    # and a single-GPU handle refuses the exchange calls
+    h = lc.lioncub_create(d, W, None, 0.9, 0.99, 1e-4, 0.1, 0, 1, lc.GRAD_BF16, 0)
+    try:
+        with pytest.raises(lc.LionCubError) as e:
+            lc.lioncub_dist_bind_buffers(h, [0] * lc.DIST_BUFFERS)
+        assert e.value.code == lc.ERR_STATE
+    finally:
+        lc.lioncub_destroy(h)
