@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) k_diagnose(const StepArgs a, lioncub
 //
 // The max-norm quantizer with stochastic rounding that the pages compare L1
 // quantization against ("Lion Cub" page, "Core claim" and the Fig. 4
-// caption: it collapses most entries of the heavy-tailed update to zero).
+// caption: on Lion's heavy-tailed update it turns most codes into zeros).
 // Per (worker, tensor): M_inf = max |c|; inv = RN(qmax / M_inf) (0 when
 // M_inf == 0); per element y = RN(|c| * inv), code = floor(y) + (u < y -
 // floor(y)), clamped to qmax, with the sign of c.  u is the top 24 bits of

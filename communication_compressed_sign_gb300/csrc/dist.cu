@@ -5,9 +5,10 @@
 // "Lion Cub: Minimizing Communication Overhead in Distributed Lion": the
 // quoted body text on the implementation (1-bit Lion Cub exchanges its packed
 // signs with an AlltoAll, the 4-bit and wider variants sum their codes with
-// an AllReduce), "What carries the argument" (a 1-bit compressed allreduce
-// tailored to majority voting; a quantized sum followed by a global sign;
-// momentum averaged on the input-embedding and output layers) and the
+// an AllReduce), "What carries the argument" (an allreduce of 1-bit words
+// built for the majority vote; the workers' quantized update vectors are
+// summed and the sum's sign is applied; the embedding and output layers
+// average their momentum) and the
 // Fig. 1 / Fig. 8 captions (1-bit and p-bit containers).
 //
 // A step is three launches around the caller's collectives:

@@ -302,9 +302,9 @@ LIONCUB_API int lioncub_diagnose(lioncub_t h, const void* const* grads, lioncub_
 /*
  * The max-norm quantizer the pages compare Eq. (1) against, as a comparator
  * of the same kind: [LC] "Core claim" (the standard max-norm quantizer Q_inf
- * collapses most entries of Lion's heavy-tailed update to zero), the Fig. 4
- * caption (Q_inf stochastic quantization clips most values to zero, giving
- * low match and flip rates) and the referee report (Q_inf rounds
+ * turns most entries of Lion's heavy-tailed update into zeros), the Fig. 4
+ * caption (its stochastic codes are mostly zero, so few signs match or
+ * flip) and the referee report (Q_inf rounds
  * stochastically).  The pages do not print Q_inf; this library reads it as:
  * per (worker, tensor) M_inf = max |c|, inv = RN(qmax / M_inf) (0 when
  * M_inf == 0), y = RN(|c| * inv), code = floor(y) + (u < y - floor(y) ? 1 :
@@ -356,8 +356,8 @@ LIONCUB_API const char* lioncub_strerror(int code);
  *
  * Source: [LC] the quoted body text on the implementation (1-bit Lion Cub
  * exchanges its packed signs with an AlltoAll; the 4-bit and wider variants
- * sum their codes with an AllReduce), "What carries the argument" (a 1-bit
- * compressed allreduce tailored to majority voting: each worker's packed
+ * sum their codes with an AllReduce), "What carries the argument" (an
+ * allreduce of 1-bit words built for the majority vote: each worker's packed
  * signs are split into chunks, the owner of a chunk takes its vote, the
  * result is gathered back; momentum averaged on the input-embedding and
  * output layers) and the Fig. 1 / Fig. 8 captions.
@@ -438,8 +438,9 @@ LIONCUB_API int lioncub_dist_plan_make(int64_t d, int W, int nranks, int rank, c
 /*
  * A handle for rank `rank` of `nranks`, holding the W/nranks local workers
  * (arguments otherwise as lioncub_create).  lioncub_bind_state then takes
- * W/nranks momenta.  The single-GPU lioncub_step, lioncub_step_host and
- * lioncub_diagnose refuse such a handle (ERR_STATE).
+ * W/nranks momenta.  The single-GPU lioncub_step, lioncub_step_host,
+ * lioncub_diagnose and lioncub_diagnose_qinf refuse such a handle
+ * (ERR_STATE).
  */
 LIONCUB_API int lioncub_dist_create(lioncub_t* out, int64_t d, int W, int nranks, int rank,
                                     const lioncub_tensor* layout, int K, float beta1, float beta2, float lr,

@@ -169,9 +169,9 @@ int lco_diagnose(int64_t d, int W, const lco_tensor* layout, int K,
 /*
  * The max-norm quantizer with stochastic rounding that the pages compare L1
  * quantization against ([LC] "Core claim": the standard max-norm quantizer
- * Q_inf collapses most entries of Lion's heavy-tailed update to zero; Fig. 4
- * caption: Q_inf stochastic quantization clips most values to zero, giving
- * low match and flip rates; the referee report: Q_inf uses stochastic
+ * Q_inf turns most entries of Lion's heavy-tailed update into zeros; the
+ * Fig. 4 caption: its stochastic codes are mostly zero, so few signs match or
+ * flip; the referee report: Q_inf uses stochastic
  * rounding).  The pages do not print it; the reading here:
  *   M_inf = max |c| over the tensor (per worker), inv = qmax / M_inf in fp32
  *   (0 when M_inf == 0), y = |c| * inv in fp32, q = floor(y) + (u < y -

@@ -547,7 +547,7 @@ def test_diagnose_tie_rate_statistics(oracle_lib):
 # ---------------------------------------------------------------------------
 # Q_inf: max-norm scaling with stochastic rounding, the comparator of the
 # diagnostics ("Lion Cub" page, "Core claim" and the Fig. 4 caption: Q_inf
-# collapses most entries of the heavy-tailed update to zero)
+# turns most of the heavy-tailed update into zero codes)
 # ---------------------------------------------------------------------------
 
 def test_splitmix64_published_outputs(oracle_lib):
