@@ -13,8 +13,9 @@ After every step each emulated rank's theta, and the momenta of its workers,
 must equal those of ``lioncub_step`` over all W workers on one GPU, bit for
 bit -- in sign mode (majority, tie alternation, the D-Lion average), in L1
 mode with 2-, 4- and 8-bit codes, with and without momentum sync -- which
-the single-GPU parity tests tie to the oracle.  A last test runs
-``DistLionCub`` through a real NCCL process group of one rank.
+the single-GPU parity tests tie to the oracle.  Two more tests run
+``DistLionCub`` itself: through a real NCCL process group of one rank, and at
+N = 2 as two processes sharing this GPU through a gloo group.
 """
 import os
 import socket
@@ -282,3 +283,75 @@ def test_exchange_call_order_and_handles(lc):
         assert e.value.code == lc.ERR_STATE
     finally:
         lc.lioncub_destroy(h)
+
+
+def _gloo_rank(rank, nranks, port, case, q):
+    try:
+        import synth as sy
+        import torch.distributed as dist
+        from communication_compressed_sign_gb300 import lioncub
+        from communication_compressed_sign_gb300.dist import DistLionCub
+        lioncub.load()
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=nranks)
+        name, W, mode, nbits, flags, sync, grad = case
+        dist_ = ("normal", 1e-3) if grad == "f32" else ("t", 3.0, 1e-3, 0.0, 1.0)
+        wl = sy.Workload(0, name, W, SMALL, grad, dist_, mode, nbits, 4, sync_interval=sync, flags=flags)
+        d, lay = wl.d, sy.abi_layout(wl.layout)
+        gcode = lioncub.GRAD_F32 if grad == "f32" else lioncub.GRAD_BF16
+        theta0 = torch.empty(d, dtype=torch.float32, device=dev)
+        sy.fill_theta_(theta0, wl)
+        opt = DistLionCub(d, W, lay, beta1=wl.beta1, beta2=wl.beta2, lr=wl.lr, wd=wl.wd, mode=mode | flags,
+                          nbits=nbits, grad_dtype=gcode, sync_interval=sync, device=dev)
+        Wl, first = opt.plan.local_workers, opt.plan.first_worker
+        theta = theta0.clone()
+        m = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(Wl)]
+        opt.bind(theta, m)
+        theta_ref = theta0.clone()
+        m_ref = [torch.zeros(d, dtype=torch.float32, device=dev) for _ in range(W)]
+        h = lioncub.lioncub_create(d, W, lay, wl.beta1, wl.beta2, wl.lr, wl.wd, mode | flags, nbits, gcode, sync)
+        grads = [torch.empty(d, dtype=sy.grad_dtype(wl), device=dev) for _ in range(W)]
+        try:
+            lioncub.lioncub_bind_state(h, theta_ref.data_ptr(), [x.data_ptr() for x in m_ref])
+            for t in range(4):
+                for j in range(W):
+                    sy.fill_grad_(grads[j], wl, t, j)
+                    grads[j][::11] = 0
+                opt.step(grads[first:first + Wl])
+                lioncub.lioncub_step(h, [g.data_ptr() for g in grads], torch.cuda.current_stream().cuda_stream)
+                torch.cuda.synchronize()
+                assert torch.equal(_bits(theta), _bits(theta_ref)), (name, rank, t)
+                for i in range(Wl):
+                    assert torch.equal(_bits(m[i]), _bits(m_ref[first + i])), (name, rank, t, i)
+        finally:
+            lioncub.lioncub_destroy(h)
+            opt.close()
+        dist.barrier()
+        dist.destroy_process_group()
+        q.put((rank, "ok"))
+    except BaseException:
+        import traceback
+        q.put((rank, traceback.format_exc()))
+
+
+@pytest.mark.parametrize("case", [("sign_sync1", 4, 0, 1, 0, 1, "bf16"), ("l1n4_sync2", 4, 1, 4, 0, 2, "f32"),
+                                  ("average", 4, 0, 1, 0x200, 0, "bf16")])
+def test_two_processes_through_torch_distributed(lc, case):
+    """DistLionCub with two ranks as two processes that share this GPU, the
+    collectives through a gloo group (which moves CUDA tensors through the
+    host, so no kernel ever waits for another process): the product's own
+    collective calls between the library's launches, at N = 2, equal to
+    lioncub_step over all W workers bit for bit."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gloo_rank, args=(r, 2, port, case, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=300) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+    bad = {r: m for r, m in res.items() if m != "ok"}
+    assert not bad, "\n".join(f"rank {r}:\n{m}" for r, m in bad.items())
