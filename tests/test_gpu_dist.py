@@ -15,7 +15,7 @@ bit -- in sign mode (majority, tie alternation, the D-Lion average), in L1
 mode with 2-, 4- and 8-bit codes, with and without momentum sync -- which
 the single-GPU parity tests tie to the oracle.  Two more tests run
 ``DistLionCub`` itself: through a real NCCL process group of one rank, and at
-N = 2 as two processes sharing this GPU through a gloo group.
+N = 2 and 4 as processes sharing this GPU through a gloo group.
 """
 import os
 import socket
@@ -335,22 +335,25 @@ def _gloo_rank(rank, nranks, port, case, q):
         q.put((rank, traceback.format_exc()))
 
 
-@pytest.mark.parametrize("case", [("sign_sync1", 4, 0, 1, 0, 1, "bf16"), ("l1n4_sync2", 4, 1, 4, 0, 2, "f32"),
-                                  ("average", 4, 0, 1, 0x200, 0, "bf16")])
-def test_two_processes_through_torch_distributed(lc, case):
-    """DistLionCub with two ranks as two processes that share this GPU, the
+@pytest.mark.parametrize("case,nranks", [(("sign_sync1", 4, 0, 1, 0, 1, "bf16"), 2),
+                                         (("l1n4_sync2", 4, 1, 4, 0, 2, "f32"), 2),
+                                         (("average", 4, 0, 1, 0x200, 0, "bf16"), 2),
+                                         (("sign_w8_sync1", 8, 0, 1, 0, 1, "bf16"), 4),
+                                         (("l1n2", 8, 1, 2, 0, 0, "bf16"), 4)])
+def test_processes_through_torch_distributed(lc, case, nranks):
+    """DistLionCub with 2 or 4 ranks as processes that share this GPU, the
     collectives through a gloo group (which moves CUDA tensors through the
     host, so no kernel ever waits for another process): the product's own
-    collective calls between the library's launches, at N = 2, equal to
-    lioncub_step over all W workers bit for bit."""
+    collective calls between the library's launches equal lioncub_step over
+    all W workers bit for bit."""
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_gloo_rank, args=(r, 2, port, case, q)) for r in range(2)]
+    procs = [ctx.Process(target=_gloo_rank, args=(r, nranks, port, case, q)) for r in range(nranks)]
     for p in procs:
         p.start()
-    res = dict(q.get(timeout=300) for _ in range(2))
+    res = dict(q.get(timeout=300) for _ in range(nranks))
     for p in procs:
         p.join(timeout=60)
     bad = {r: m for r, m in res.items() if m != "ok"}
