@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(256, kMinBlocks) k_reduce_apply_staged(const S
     }
     // L2 is asked for the theta of the block `ahead` blocks later (about one
     // resident wave: the block that takes this slot next): measured 1.0-1.5 %
-    // faster on the 16-worker and 1.3B workloads, neutral on GPT-2 small
-    {
+    // faster with signs from 16 workers and with 2-bit codes, neutral with
+    // signs from 8; with 4-bit codes it was 2 % slower, so wider codes skip it
+    if constexpr (NB <= 2) {
         const int64_t pblk = (static_cast<int64_t>(blockIdx.x) + ahead) * (kStagedGroups * kGroupElems);
 #pragma unroll
         for (int q = 0; q < kStagedGroups; ++q) {
