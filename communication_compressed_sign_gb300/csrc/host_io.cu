@@ -6,7 +6,9 @@
 // next step's gradient upload, which runs at the same time.  Measured on the
 // 124M-parameter, 8-worker layout (2.0 GB up, 0.5 GB down per step), the
 // pipelined data movement took 9.79 ms per step this way against 10.09 ms
-// with both directions on copy engines.
+// with both directions on copy engines.  At 1.4B parameters (22.7 GB up,
+// 5.7 GB down) the SM stores ran at 134.5 GB/s beside uploads that kept 207
+// GB/s, while a copy-engine download cut the uploads to 152 GB/s.
 #include "host_io.h"
 
 namespace lc {

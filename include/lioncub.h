@@ -159,7 +159,7 @@ typedef struct {
 /* Kernels whose launches lioncub_profile_read reports. */
 enum {
     LIONCUB_KERNEL_COMPRESS = 0,     /* c, sign bits or Q1 codes, momentum, sync */
-    LIONCUB_KERNEL_M1 = 1,           /* per-tile fp64 sums of |c| (L1 mode)      */
+    LIONCUB_KERNEL_M1 = 1,           /* per-tile compensated sums of |c| (L1)   */
     LIONCUB_KERNEL_M1_FINAL = 2,     /* per-tensor M1 and 1/M1 scale (L1 mode)   */
     LIONCUB_KERNEL_REDUCE_APPLY = 3, /* W-way vote / integer sum, sign, theta    */
     LIONCUB_KERNEL_DIAGNOSE = 4,     /* lioncub_diagnose's counting pass          */

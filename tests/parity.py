@@ -268,11 +268,14 @@ def _assert_bounds(rep: ParityReport, l1: bool, W: int, t: int):
         assert rep.m_mismatch == 0, f"step {t}: momentum differs: {rep}"
 
 
-def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_flags: int = 0):
+def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_flags: int = 0,
+                    zero_stride: int = 0):
     """Warm the state up with `warm_steps` GPU steps, then compare
     lioncub_diagnose for the next step's gradients with the oracle's
-    diagnostics on the named whole tensors (every field exact).  Returns the
-    GPU records of those tensors."""
+    diagnostics on the named whole tensors (every field exact).  With
+    zero_stride > 0 every zero_stride-th gradient is 0 at every step, so the
+    momentum and the update vector stay exactly 0 there.  Returns the GPU
+    records of those tensors."""
     import torch
 
     dev = torch.device("cuda", 0)
@@ -289,13 +292,17 @@ def run_diag_parity(wl: synth.Workload, tensor_names, warm_steps: int = 2, mode_
     try:
         lc.lioncub_bind_state(h, theta.data_ptr(), [x.data_ptr() for x in m])
         s = torch.cuda.current_stream().cuda_stream
-        for t in range(warm_steps):
+        def fill(t):
             for i in range(W):
                 synth.fill_grad_(grads[i], wl, t, i)
+                if zero_stride:
+                    grads[i][::zero_stride] = 0
+
+        for t in range(warm_steps):
+            fill(t)
             lc.lioncub_step(h, [g.data_ptr() for g in grads], s)
         t = warm_steps
-        for i in range(W):
-            synth.fill_grad_(grads[i], wl, t, i)
+        fill(t)
         K = len(wl.layout)
         out = torch.zeros(K * lc.DIAG_BYTES, dtype=torch.uint8, device=dev)
         theta_before = theta.clone()

@@ -419,6 +419,19 @@ def test_diagnose_small(mode, nbits, flags):
     parity.run_diag_parity(wl, {n for (n, _, _, _) in layout}, warm_steps=3, mode_flags=flags)
 
 
+@pytest.mark.parametrize("W", [6, 8])
+@pytest.mark.parametrize("warm", [2, 3])
+@pytest.mark.parametrize("mode,nbits", [(0, 1), (1, 2), (1, 4)])
+def test_diagnose_exact_zero_updates(mode, nbits, warm, W):
+    """Elements whose update vector is exactly 0 at both step parities (their
+    vote is the step's zero sign in sign mode, code 0 in L1 mode), with a
+    power-of-two and another worker count (the mean's two code paths)."""
+    layout = _multi_layout(sync=False)
+    wl = _small(synth.layout_total(layout), W, "bf16", mode, nbits, layout=layout)
+    res = parity.run_diag_parity(wl, {n for (n, _, _, _) in layout}, warm_steps=warm, zero_stride=5)
+    assert any(r["dropped"] + r["spurious"] > 0 for _, r in res) or mode == 1
+
+
 def test_diagnose_full_size_workloads():
     for key, names in ((2, {"wpe", "h5.mlp.c_fc.b", "ln_f.w"}), (3, {"wpe", "h0.attn.c_attn.b", "ln_f.b"}),
                        (4, {"h3.attn.c_proj.w", "ln_f.w"})):
