@@ -395,7 +395,14 @@ def run_gpu(args, wl: synth.Workload):
     # diagnostics pass (not part of the step): timed separately when asked
     diag = run_diagnose(args, wl, h, dev, stream, gptrs[0]) if args.diagnose else None
 
-    # end to end: host gradients in, host theta out, through lioncub_step_host
+    # end to end: host gradients in, host theta out, through lioncub_step_host.
+    # The device-resident leg's gradient buffers are released first: that leg
+    # is done, and the host step stages its own copies (45 GB of idle device
+    # buffers on the 1.3B workload measured up to 1.6x slower host steps on
+    # some boxes, with a periodic stall).
+    gptrs = None
+    grads = None
+    torch.cuda.empty_cache()
     e2e = None if args.no_e2e else run_e2e(args, wl, h, dev, stream)
 
     # the device status word (bounded waits that gave up, guard bands around
@@ -408,7 +415,7 @@ def run_gpu(args, wl: synth.Workload):
         raise RuntimeError(f"device status word is {int(status.item())} after the timed steps")
 
     lc.lioncub_destroy(h)
-    del grads, m, theta, flush_buf
+    del m, theta, flush_buf
     torch.cuda.empty_cache()
 
     result = {
@@ -662,14 +669,18 @@ def run_e2e(args, wl, h, dev, stream):
     torch.cuda.synchronize(dev)
     barrier(dev)
     t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    # an event after each step (after its theta download) gives the spread
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
     for s in range(args.steps):
         lc.lioncub_step_host(h, ptrs[s % 2], theta_host.data_ptr(), sp)
-    e1.record(stream)
+        ev[s + 1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
-    ms = reduce_max(e0.elapsed_time(e1) / args.steps, dev)
+    ms = reduce_max(ev[0].elapsed_time(ev[-1]) / args.steps, dev)
+    per = sorted(ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps))
+    spread = {"median": per[len(per) // 2], "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10],
+              "max": per[-1]}
     ws, _, _ = dist_env()
     G = 4 if wl.grad == "f32" else 2
     h2d = W * d * G
@@ -679,6 +690,7 @@ def run_e2e(args, wl, h, dev, stream):
             x.close()
     theta_host.close()
     return {"value": ws * d / (ms * 1e-3), "unit": "param-elements/s", "ms_per_step": ms,
+            "ms_per_step_spread": spread,
             "wall_ms_per_step": wall * 1e3 / args.steps,
             "host_cpus_bound": sorted(cpus & saved) if cpus and cpus & saved else None,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * d,

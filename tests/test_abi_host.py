@@ -84,7 +84,7 @@ def test_create_validation_codes(lc):
     assert h.value is None
 
 
-def _layout_verdict(d, layout):
+def _layout_expected(d, layout):
     """The documented layout contract, written independently of the library:
     tensors tile [0, d) in order, every offset a multiple of 32 (checked first
     for each tensor), non-negative sizes, known flags only."""
@@ -130,7 +130,7 @@ def test_create_layout_fuzz(lc):
             off = o + max(n, 0)
         d = sum(max(n, 0) for (_, n, _) in layout) + (int(rng.integers(-2, 3)) if rng.random() < 0.1 else 0)
         d = max(d, 0)
-        want = _layout_verdict(d, layout)
+        want = _layout_expected(d, layout)
         counts[want] += 1
         arr = (lc.Tensor * K)(*[lc.Tensor(*t) for t in layout])
         h = ctypes.c_void_p()
