@@ -813,7 +813,15 @@ def main(argv=None):
     else:
         res = run_gpu(args, wl)
     if res is not None:
-        print(json.dumps(res))
+        # libraries that print through C stdio (NCCL's version and debug
+        # lines) are flushed first, so the result is the last line
+        try:
+            import ctypes
+            ctypes.CDLL(None).fflush(None)
+        except (OSError, AttributeError):
+            pass
+        sys.stdout.flush()
+        print(json.dumps(res), flush=True)
 
 
 if __name__ == "__main__":
