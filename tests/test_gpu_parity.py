@@ -432,6 +432,21 @@ def test_diagnose_exact_zero_updates(mode, nbits, warm, W):
     assert any(r["dropped"] + r["spurious"] > 0 for _, r in res) or mode == 1
 
 
+@pytest.mark.parametrize("warm", [2, 3])
+def test_diagnose_many_tiles_odd_workers(warm):
+    """Sign-mode diagnostics on more tiles than the persistent grid holds
+    (each block loops over several tiles and asks L2 for the next), with a
+    worker count that is not a power of two (the mean by division) and
+    ragged tensors, every tensor checked whole at both step parities."""
+    sizes = [1_000_003 // 32 * 32, 2048 * 700 + 96, 32, 2_100_000 // 32 * 32, 4096 + 480]
+    layout, off = [], 0
+    for k, n in enumerate(sizes):
+        layout.append((f"t{k}", off, n, 0))
+        off += n
+    wl = _small(off, 6, "bf16", 0, 1, layout=layout)
+    parity.run_diag_parity(wl, {n for (n, _, _, _) in layout}, warm_steps=warm, zero_stride=97)
+
+
 def test_diagnose_full_size_workloads():
     for key, names in ((2, {"wpe", "h5.mlp.c_fc.b", "ln_f.w"}), (3, {"wpe", "h0.attn.c_attn.b", "ln_f.b"}),
                        (4, {"h3.attn.c_proj.w", "ln_f.w"})):
