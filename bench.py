@@ -152,6 +152,16 @@ def reduce_max(value: float, device=None) -> float:
     return float(t.item())
 
 
+def reduce_min(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return float(t.item())
+
+
 def barrier(device=None):
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -639,6 +649,44 @@ def gpu_local_cpus(index: int):
         return None
 
 
+def host_memory_available() -> int:
+    """Bytes this process may still allocate on the host: MemAvailable, or
+    the cgroup's remaining limit when that is lower."""
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            lim = f.read().strip()
+        with open("/sys/fs/cgroup/memory.current") as f:
+            cur = int(f.read().strip())
+        if lim != "max":
+            left = int(lim) - cur
+            avail = left if avail is None else min(avail, left)
+    except (OSError, ValueError):
+        pass
+    return avail if avail is not None else 1 << 62
+
+
+def e2e_host_layout(W: int, grad_bytes: int, theta_bytes: int, ranks_here: int, avail: int):
+    """How the host gradients of the host-buffer leg are laid out, so that
+    every rank on this node fits in 60 % of the available host memory:
+    two sets of W buffers (steps alternate), one set, or one buffer that all W
+    workers read (the bytes copied per step are the same in every case).
+    Returns (sets, distinct buffers per set) or None when even that does not
+    fit."""
+    budget = 0.6 * avail
+    for sets, per_set in ((2, W), (1, W), (1, 1)):
+        if ranks_here * (sets * per_set * grad_bytes + theta_bytes) <= budget:
+            return sets, per_set
+    return None
+
+
 def run_e2e(args, wl, h, dev, stream):
     """K steps through lioncub_step_host: every step copies the W gradient
     buffers from pinned host memory to the device and theta back."""
@@ -646,6 +694,18 @@ def run_e2e(args, wl, h, dev, stream):
     from communication_compressed_sign_gb300 import lioncub as lc
     d, W = wl.d, wl.W
     gdt = synth.grad_dtype(wl)
+    G = 4 if wl.grad == "f32" else 2
+    ws, _, _ = dist_env()
+    ranks_here = int(os.environ.get("LOCAL_WORLD_SIZE", ws))
+    # every rank reads the host memory before any of them allocates, and all
+    # take the smallest reading, so they choose the same layout
+    barrier(dev)
+    avail = int(reduce_min(float(host_memory_available()), dev))
+    layout = e2e_host_layout(W, d * G, 4 * d, ranks_here, avail)
+    if layout is None:
+        return {"value": None, "unit": "param-elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "skipped": f"host memory: {ranks_here} ranks x one gradient buffer and theta do not fit"}
+    nsets, per_set = layout
     # page-locked buffers from the library's allocator (torch's caching pinned
     # allocator measured up to 40 % slower host-to-device at the 1.3B size),
     # on the GPU's own NUMA node: allocate (first touch) from a thread bound
@@ -654,15 +714,16 @@ def run_e2e(args, wl, h, dev, stream):
     saved = os.sched_getaffinity(0)
     if cpus and cpus & saved:
         os.sched_setaffinity(0, cpus & saved)
-    host = [[lc.HostBuffer(d, gdt) for _ in range(W)] for _ in range(2)]
+    host = [[lc.HostBuffer(d, gdt) for _ in range(per_set)] for _ in range(nsets)]
     tmp = torch.empty(d, dtype=gdt, device=dev)
-    for s in range(2):
-        for i in range(W):
+    for s in range(nsets):
+        for i in range(per_set):
             synth.fill_grad_(tmp, wl, s, i)
             host[s][i].tensor.copy_(tmp)
     del tmp
     theta_host = lc.HostBuffer(d, torch.float32)
-    ptrs = [[x.data_ptr() for x in host[s]] for s in range(2)]
+    # worker i of step s reads host[s % nsets][i % per_set]
+    ptrs = [[host[s % nsets][i % per_set].data_ptr() for i in range(W)] for s in range(2)]
     sp = stream.cuda_stream
     for s in range(max(1, args.warmup)):
         lc.lioncub_step_host(h, ptrs[s % 2], theta_host.data_ptr(), sp)
@@ -681,8 +742,6 @@ def run_e2e(args, wl, h, dev, stream):
     per = sorted(ev[s].elapsed_time(ev[s + 1]) for s in range(args.steps))
     spread = {"median": per[len(per) // 2], "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10],
               "max": per[-1]}
-    ws, _, _ = dist_env()
-    G = 4 if wl.grad == "f32" else 2
     h2d = W * d * G
     os.sched_setaffinity(0, saved)
     for row in host:
@@ -695,6 +754,8 @@ def run_e2e(args, wl, h, dev, stream):
             "host_cpus_bound": sorted(cpus & saved) if cpus and cpus & saved else None,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * d,
             "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
+            "host_gradient_buffers": f"{nsets} set(s) of {per_set} (steps alternate between sets; "
+                                     f"worker i reads buffer i mod {per_set})",
             "api": "lioncub_step_host (page-locked host buffers from lioncub_host_alloc; uploads overlap "
                    "the previous step)"}
 
