@@ -16,16 +16,17 @@
 // momentum spread is mean = (sum m_i) / W, var = (sum (m_i - mean)^2) / W,
 // std = sqrt(var), all in fp32 with one rounding per operation.
 //
-// One block per tile; each thread takes 8 elements and loops over the
-// workers, software-pipelined on full groups (a second loop re-reads the
-// momenta for the variance; the first loop reads them with the default cache
-// policy so that the second finds them in L2).  The pass is bound by
-// instruction issue more than by DRAM, so the per-element work outside the
-// worker loops is kept small: counts packed into two words and summed by warp
-// reductions, the maximum taken over sums of squares before the one division
-// and square root of a block.  Per-tensor totals are combined with integer
-// atomics (exact, order-free) and the maximum with an integer atomicMax on
-// the non-negative float's bits.
+// One block per tile (with sign votes: resident blocks that loop over the
+// tiles); each thread takes 8 elements and loops over the workers,
+// software-pipelined on full groups (a second loop re-reads the momenta for
+// the variance; the first loop reads them with the default cache policy so
+// that the second finds them in L2).  The pass sits near the instruction-issue
+// limit, so the per-element work outside the worker loops is kept small:
+// counts packed into two words and summed by warp reductions, the maximum
+// taken over sums of squares before the one division and square root of a
+// block.  Per-tensor totals are combined with integer atomics (exact,
+// order-free) and the maximum with an integer atomicMax on the non-negative
+// float's bits.
 #include "device_common.cuh"
 
 namespace lc {
